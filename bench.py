@@ -1,0 +1,547 @@
+#!/usr/bin/env python3
+"""Benchmark of the hierarchical KV cache resolver on GB300: top-k selections resolved per second.
+
+A step is one decode step of a synthetic workload: hs_step_begin plus one hs_resolve per layer for every
+request (captured once per step of the workload's selection sequence into a CUDA graph and replayed). The
+sequence starts from an empty cache, so the first step is the all-miss cold start; when K exceeds the sequence
+the pool is reset (outside the timed intervals) and the sequence restarts. One selection = one request-layer's
+top-k list for one step.
+
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the launching stream with a 256 MiB L2
+flush between steps (outside the events), barrier + synchronize around the whole region, max over ranks. Clocks
+are sampled with nvidia-smi during the timed region.
+
+Roofline (the slower of two terms): miss-row bytes over the measured host link, and metadata + hot-buffer bytes
+over HBM (measured copy peak). The dominant kernel's duration comes from events around each hs_resolve launch
+in a second pass over the same steps.
+
+Also reported: e2e (the same steps through the public API with the selection copied in from pinned host memory
+and out_slots copied back inside the timed region), a no-IO run (misses sourced from an HBM copy of the pool),
+and the CPU oracle on a bounded sample (``cpu_baseline``).
+
+`--impl reference` times the CPU oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workload as wl  # noqa: E402
+
+METRIC = "top-k selections resolved/s"
+UNIT = "selections/s"
+FLUSH_BYTES = 256 << 20
+
+
+def describe(w: wl.Workload) -> str:
+    sel = "shared by all layers" if w.shared_across_layers else "per layer"
+    return (f"{w.name}: {w.requests} requests x {w.layers} layers, ctx {w.ctx}, top-k {w.topk} ({sel}), "
+            f"{w.slots} hot slots, {w.row_bytes}-B rows, {w.steps} steps")
+
+
+def mem_available() -> int:
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def choose_host_layers(w: wl.Workload) -> int:
+    """All layers get their own host pool when it fits in half of the available host memory; otherwise every
+    layer reads one shared pool (host_layer_stride 0). Loads use ld.global.cv, so a shared pool still sends
+    every miss over the link."""
+    if w.layers == 1:
+        return 1
+    return w.layers if w.host_bytes() < 0.5 * mem_available() else 1
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        time.sleep(0.15)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def meta_bytes_per_launch(w: wl.Workload, batch: int) -> int:
+    """Metadata bytes of one resolve launch that do not depend on hits/misses: selection read, tok2slot gather,
+    out_slots write (4k each) and the stamp + slot-token reads (8H), per request-layer."""
+    return batch * (12 * w.topk + 8 * w.slots)
+
+
+class GpuRun:
+    """One pool for a workload, its per-step graphs, and the measurement passes."""
+
+    def __init__(self, w: wl.Workload, noio: bool = False, prefetch: bool = False, host: object = None,
+                 host_layers: int | None = None):
+        import torch
+
+        import hierarchical_sparse_attention_hs_gb300 as hs
+
+        self.torch, self.hs, self.w = torch, hs, w
+        self.noio, self.prefetch = noio, prefetch
+        self.host_layers = choose_host_layers(w) if host_layers is None else host_layers
+        self.buf = hs.PoolBuffers(w.layers, w.requests, w.ctx, w.slots, w.topk, w.row_bytes,
+                                  host_layers=self.host_layers, noio=noio, host=host)
+        if host is None:
+            wl.fill_host_pool(w, self.buf.host.ptr, self.host_layers)
+        if noio:
+            self.buf.upload_noio()
+        self.pool = self.buf.create()
+        sel = wl.gen_selections(w)  # [steps][selection layers][B][k]
+        self.sel_host = sel
+        self.sel = torch.from_numpy(sel).cuda()
+        self.out = torch.empty((w.layers, w.requests, w.topk), dtype=torch.int32, device="cuda")
+        self.stream = torch.cuda.Stream()
+        self.side = torch.cuda.Stream() if prefetch else None
+        self.flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+        self.graphs = [self._capture(s) for s in range(w.steps)]
+        torch.cuda.synchronize()
+
+    def _lsel(self, l):
+        return 0 if self.w.shared_across_layers else l
+
+    def enqueue(self, s, topk=None, events=None):
+        """Enqueue decode step s on self.stream (topk: device selections [Lsel][B][k] to use instead of the
+        pre-staged ones). events: optional list receiving (start, end) CUDA events around each resolve launch."""
+        torch, hs, w = self.torch, self.hs, self.w
+        st = self.stream
+        src = self.sel[s] if topk is None else topk
+        hs.hs_step_begin(self.pool, st)
+        if not self.prefetch:
+            for l in range(w.layers):
+                if events is not None:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(st)
+                hs.hs_resolve(self.pool, l, w.requests, src[self._lsel(l)], w.topk, self.out[l], st)
+                if events is not None:
+                    e1.record(st)
+                    events.append((e0, e1))
+            return
+        # exact layer-wise prefetch: layer l+1 resolves on the side stream while layer l resolves here
+        side = self.side
+        ev0 = torch.cuda.Event()
+        ev0.record(st)
+        side.wait_event(ev0)
+        done = [None] * w.layers
+        for l in range(1, w.layers):
+            hs.hs_prefetch(self.pool, l, w.requests, src[self._lsel(l)], w.topk, side)
+            done[l] = torch.cuda.Event()
+            done[l].record(side)
+        for l in range(w.layers):
+            if done[l] is not None:
+                st.wait_event(done[l])
+            hs.hs_resolve(self.pool, l, w.requests, src[self._lsel(l)], w.topk, self.out[l], st)
+        evj = torch.cuda.Event()
+        evj.record(side)
+        st.wait_event(evj)
+
+    def _capture(self, s):
+        g = self.torch.cuda.CUDAGraph()
+        with self.torch.cuda.graph(g, stream=self.stream):
+            self.enqueue(s)
+        return g
+
+    def launches_per_step(self) -> int:
+        return 1 + self.w.layers + (self.w.layers - 1 if self.prefetch else 0)
+
+    def flush(self):
+        with self.torch.cuda.stream(self.stream):
+            self.flush_buf.fill_(1)
+
+    def reset(self):
+        self.hs.hs_pool_reset(self.pool, self.stream)
+
+    def run_steps(self, k_steps: int, start: int = 0, timed: bool = True):
+        """Replay k_steps decode steps starting at sequence position `start`; returns per-step ms (or [])."""
+        torch = self.torch
+        times = []
+        pos = start
+        for _ in range(k_steps):
+            if pos == self.w.steps:
+                pos = 0
+                self.reset()
+            self.flush()
+            if timed:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(self.stream)
+            with torch.cuda.stream(self.stream):
+                self.graphs[pos].replay()
+            if timed:
+                e1.record(self.stream)
+                times.append((pos, e0, e1))
+            pos += 1
+        self.stream.synchronize()
+        return [(p, a.elapsed_time(b)) for p, a, b in times], pos
+
+    def kernel_pass(self, k_steps: int):
+        """Eager replay of the same steps with events around every hs_resolve launch. Returns (sum of kernel ms,
+        number of launches, counters (hits, misses, evictions, bytes) summed over layers and over the steps)."""
+        torch = self.torch
+        self.reset()
+        evs = []
+        totals = np.zeros(4, dtype=np.int64)
+        pos = 0
+        for _ in range(k_steps):
+            if pos == self.w.steps:
+                pos = 0
+                self.stream.synchronize()
+                totals += self.counters_total()
+                self.reset()
+            self.flush()
+            with torch.cuda.stream(self.stream):
+                self.enqueue(pos, events=evs)
+            pos += 1
+        self.stream.synchronize()
+        totals += self.counters_total()
+        ms = sum(a.elapsed_time(b) for a, b in evs)
+        return ms, len(evs), totals
+
+    def counters_total(self) -> np.ndarray:
+        return self.buf.view("counters").cpu().numpy().astype(np.int64).sum(axis=0)
+
+    def e2e_pass(self, k_steps: int):
+        """Public-API loop with host buffers: per step, copy the selections in from pinned host memory, run the
+        step's graph, copy out_slots back to pinned host memory; events bracket the whole step."""
+        torch = self.torch
+        w = self.w
+        self.reset()
+        host_sel = torch.from_numpy(self.sel_host).pin_memory()  # [steps][Lsel][B][k]
+        host_out = torch.empty(tuple(self.out.shape), dtype=torch.int32).pin_memory()
+        times = []
+        pos = 0
+        for _ in range(k_steps):
+            if pos == w.steps:
+                pos = 0
+                self.reset()
+            self.flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            with torch.cuda.stream(self.stream):
+                self.sel[pos].copy_(host_sel[pos], non_blocking=True)
+                self.graphs[pos].replay()
+                host_out.copy_(self.out, non_blocking=True)
+            e1.record(self.stream)
+            times.append((e0, e1))
+            pos += 1
+        self.stream.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in times)
+        h2d = self.sel[0].numel() * 4
+        d2h = self.out.numel() * 4
+        return ms, h2d, d2h
+
+    def close(self):
+        self.buf.close()
+
+
+def measure_link(hs, torch, host_ptr: int, nbytes: int) -> tuple:
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    zc, cp = hs.hs_probe_link(host_ptr, dev, nbytes, 5)
+    del dev
+    return zc, cp
+
+
+def cpu_baseline(w: wl.Workload, budget_s: float = 12.0) -> dict:
+    """The CPU oracle, single-threaded, on a bounded sample of the same workload (request-layers of layer 0,
+    with hot rows tracked in host memory, steps in order from the cold start until the time budget)."""
+    import oracle
+
+    reqs = w.requests
+    sel = wl.gen_selections(w, layers=(0, 1), requests=(0, reqs))
+    host = np.stack([wl.rows(w, 0, b) for b in range(reqs)])
+    pool = oracle.OraclePool(w.ctx, w.slots, w.row_bytes, 1, reqs, track_rows=True)
+    t0 = time.perf_counter()
+    n = 0
+    s = 0
+    while s < w.steps and time.perf_counter() - t0 < budget_s:
+        pool.step_begin()
+        pool.resolve(0, sel[s, 0], host)
+        n += reqs
+        s += 1
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"layer 0 of {w.name}, {reqs} requests, steps 0..{s - 1} from the cold start ({n} selections, "
+                      f"hot rows tracked, {dt:.1f} s single-threaded)"}
+
+
+def max_over_ranks(ms: float, dist=None) -> float:
+    """The slowest rank's time (every rank processes the same number of units)."""
+    if dist is None:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(world: int, units_per_rank: int, max_ms: float) -> float:
+    """Whole-job throughput: all ranks' units over the slowest rank's time (weak scaling)."""
+    return world * units_per_rank / (max_ms / 1e3)
+
+
+def run_reference(args) -> int:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+
+    w = wl.WORKLOADS[args.workload]
+    reqs = w.requests
+    sel = wl.gen_selections(w, layers=(0, 1), requests=(0, reqs))
+    host = np.stack([wl.rows(w, 0, b) for b in range(reqs)])
+    layers_per_step = max(1, min(w.layers, args.ref_layers))
+
+    def one_step(pool, s):
+        pool.step_begin()
+        for l in range(layers_per_step):
+            pool.resolve(l, sel[s % w.steps, 0], host)
+
+    pool = oracle.OraclePool(w.ctx, w.slots, w.row_bytes, layers_per_step, reqs, track_rows=True)
+    for s in range(args.warmup):
+        one_step(pool, s)
+    pool = oracle.OraclePool(w.ctx, w.slots, w.row_bytes, layers_per_step, reqs, track_rows=True)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        if s and s % w.steps == 0:
+            pool = oracle.OraclePool(w.ctx, w.slots, w.row_bytes, layers_per_step, reqs, track_rows=True)
+        one_step(pool, s)
+    dt = time.perf_counter() - t0
+    n = args.steps * reqs * layers_per_step
+    value = n / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": describe(w), "sample": f"{layers_per_step} layer(s) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} decode steps of {layers_per_step} layer(s) x {reqs} requests of "
+                                   f"{w.name}, hot rows tracked, single-threaded"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args) -> int:
+    import torch
+
+    import hierarchical_sparse_attention_hs_gb300 as hs
+    from hierarchical_sparse_attention_hs_gb300 import build as hs_build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    if rank == 0:
+        hs_build.build()
+    if dist:
+        dist.barrier()
+    hs.load()
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    hbm_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    w = wl.WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    run = GpuRun(w, prefetch=args.prefetch)
+    # warm-up, then a cold start for the timed region
+    run.run_steps(W, timed=False)
+    run.reset()
+    run.stream.synchronize()
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    with ClockSampler(local) as clk:
+        per_step, _ = run.run_steps(K)
+        barrier()
+    step_ms = [ms for _, ms in per_step]
+    total_ms = max_over_ranks(sum(step_ms), dist)
+    sel_per_step = w.layers * w.requests
+    value = aggregate_rate(world, K * sel_per_step, total_ms)
+
+    # kernel-level pass: events around each hs_resolve launch, same steps, same flushes
+    kern_ms, n_launch, tot = run.kernel_pass(K)
+    hits, misses, evictions, miss_bytes = (int(x) for x in tot)
+    link_zc, link_cp = measure_link(hs, torch, run.buf.host.ptr, min(run.buf.host.nbytes, 1 << 30) // 16 * 16)
+    link_peak = max(link_zc, link_cp)
+    meta = n_launch * meta_bytes_per_launch(w, w.requests) + 4 * hits + 16 * misses
+    hbm_bytes = meta + miss_bytes
+    t_link = miss_bytes / (link_peak * 1e9)
+    t_hbm = hbm_bytes / (hbm_peak * 1e9)
+    kern_s = kern_ms / 1e3
+    bound = "host_link" if t_link >= t_hbm else "hbm"
+    roofline = {
+        "bound": bound,
+        "achieved": (miss_bytes / kern_s / 1e9) if bound == "host_link" else (hbm_bytes / kern_s / 1e9),
+        "peak": link_peak if bound == "host_link" else hbm_peak,
+        "unit": "GB/s",
+        "frac": max(t_link, t_hbm) / kern_s,
+        "traffic": None,
+        "kernel": "hs_resolve_kernel",
+        "kernel_ms_per_launch": kern_ms / n_launch,
+        "launches": n_launch,
+        "algorithmic_bytes_per_launch": {"link": miss_bytes / n_launch, "hbm": hbm_bytes / n_launch},
+        "peak_source": f"host link measured in this run (zero-copy {link_zc:.1f}, memcpy {link_cp:.1f} GB/s); "
+                       f"HBM {hbm_peak:.1f} GB/s {hbm_src}",
+    }
+
+    # end to end through the public API with host buffers
+    e2e_ms, h2d, d2h = run.e2e_pass(K)
+    e2e_ms = max_over_ranks(e2e_ms, dist)
+    e2e = {"value": aggregate_rate(world, K * sel_per_step, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+    host = run.buf.host
+    run.buf.host = None
+    run.close()
+    torch.cuda.empty_cache()
+
+    # no-IO mode on the same workload: misses sourced from an HBM copy of the pool
+    noio = None
+    if not args.skip_noio:
+        nrun = GpuRun(w, noio=True, prefetch=args.prefetch, host=host, host_layers=run.host_layers)
+        nrun.run_steps(W, timed=False)
+        nrun.reset()
+        nper, _ = nrun.run_steps(K)
+        nms = sum(ms for _, ms in nper)
+        nk_ms, nk_launch, _ = nrun.kernel_pass(K)
+        n_hbm = meta + 2 * miss_bytes
+        nms = max_over_ranks(nms, dist)
+        noio = {"value": aggregate_rate(world, K * sel_per_step, nms), "unit": UNIT, "ms_per_step": nms / K,
+                "kernel_ms_per_launch": nk_ms / nk_launch,
+                "roofline": {"bound": "hbm", "achieved": n_hbm / (nk_ms / 1e3) / 1e9, "peak": hbm_peak,
+                             "unit": "GB/s", "frac": (n_hbm / (hbm_peak * 1e9)) / (nk_ms / 1e3)}}
+        nrun.buf.host = None
+        nrun.close()
+    host.close()
+
+    clocks = clk.summary()
+    cold = [ms for p, ms in per_step if p == 0]
+    steady = [ms for p, ms in per_step if p != 0]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int32", "data": "synthetic",
+        "config": {"workload": describe(w), "parallelism": f"replicas x{world} (independent requests per GPU)",
+                   "l2": "flushed between steps (256 MiB write)",
+                   "host_pool": ("one pool per layer" if run.host_layers == w.layers else
+                                 "layers share one host pool (host_layer_stride 0); every miss still crosses the link"),
+                   "graphs": "one CUDA graph per decode step", "prefetch": bool(args.prefetch)},
+        "selected_entries_per_s": value * w.topk,
+        "miss_gbs": miss_bytes / (total_ms / 1e3) / 1e9 * world,
+        "cold_step_ms": statistics.mean(cold) if cold else None,
+        "steady_step_ms": statistics.mean(steady) if steady else None,
+        "roofline": roofline,
+        "noio": noio,
+        "e2e": e2e,
+        "gpu_launches": K * run.launches_per_step(),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["hs", "reference"], default="hs")
+    ap.add_argument("--workload", choices=list(wl.WORKLOADS), default="dsa")
+    ap.add_argument("--prefetch", action="store_true", help="layer-wise prefetch on a second stream")
+    ap.add_argument("--skip-noio", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-layers", type=int, default=1, help="reference arm: layers resolved per step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

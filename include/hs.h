@@ -1,0 +1,184 @@
+/*
+ * hs.h -- C ABI of the hierarchical KV cache resolver for top-k sparse-attention decoding (GB300, sm_103a).
+ *
+ * The method is the per-layer selection resolution of "HiSparse: Scaling Sparse-Attention Decoding with
+ * Hierarchical KV Cache Management" (Abstract): each request keeps its full KV history in host memory and a
+ * small fixed-size GPU cache; one fused CUDA kernel per layer resolves the layer's top-k selections -- hit
+ * detection, LRU replacement and host-to-device fetches -- inside the decode CUDA graph; models that share
+ * selections across layers prefetch the next layer exactly. The "HiSparse" knowledge card (Timeline) adds that
+ * only the missing rows that hit the top-k are back-filled into the request's hot buffer, and the "Hybrid
+ * HiSparse" card (Timeline) that the single-pass fused kernel is CUDA-graph capturable.
+ *
+ * Cache instance. One request-layer (layer l, request b) owns `slots` hot rows of `row_bytes` bytes and three
+ * int32 arrays in device memory: tok2slot[ctx] (slot holding token t, or -1), slot_tok[slots] (token in slot v,
+ * or -1) and slot_stamp[slots] (decode step of the slot's last hit or fill, 0 = never used).
+ *
+ * Policy of one resolve call at decode step s, for the selection S = topk_idx[b][0..k):
+ *   - a negative entry is padding (its out_slot is -1, it touches nothing);
+ *   - if S holds a token >= ctx or a token twice, the row is rejected: its out_slots are all -1, nothing
+ *     changes, and the sticky device error word gets HS_DEVERR_RANGE / HS_DEVERR_DUP;
+ *   - hits (tok2slot[t] >= 0) take stamp s;
+ *   - misses, in ascending token order, take the victims: the slots not hit by this call with the smallest
+ *     (stamp, slot index), in that order; the victim's old token is unmapped, the miss token mapped, the
+ *     slot stamped s, and the token's row copied from the host pool into the slot;
+ *   - out_slots[b][i] = slot now holding topk_idx[b][i], in input order.
+ *
+ * Ownership: every byte of host and device memory is the caller's. The library allocates nothing on the hot
+ * path; it keeps only the small opaque hs_pool struct on the host.
+ *
+ * Errors: functions return HS_OK (0) or a negative HS_ERR_* code. Argument errors never launch anything. Input
+ * errors that only the device can see (a bad token) never trap: they set bits of the device error word, read
+ * with hs_get_error.
+ *
+ * Streams and graphs: hs_pool_create, hs_pool_reset, hs_step_begin, hs_resolve and hs_prefetch only enqueue work
+ * on the given stream (no host synchronisation) and can be captured into a CUDA graph. The kernels use
+ * programmatic dependent launch: each waits for the preceding kernel in its stream before touching memory.
+ * Pointers, batch and k are baked into a captured graph; refill topk_idx in place between replays.
+ * The hs_get_* readers synchronise the device. No function is thread-safe on the same pool.
+ */
+#ifndef HS_H_
+#define HS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers; pass 0 for the legacy default stream. */
+typedef struct CUstream_st *hs_stream_t;
+
+typedef struct hs_pool hs_pool;
+
+/* Return codes. */
+#define HS_OK 0
+#define HS_ERR_INVALID_ARG (-1) /* bad pointer, size, alignment, layer, batch or k; nothing launched */
+#define HS_ERR_CUDA (-2)        /* a CUDA runtime call or launch failed */
+#define HS_ERR_NOT_MAPPED (-3)  /* host_pool is not page-locked, device-mapped memory */
+#define HS_ERR_NO_MEMORY (-4)   /* host struct allocation failed */
+#define HS_ERR_UNSUPPORTED (-5) /* geometry needs more shared memory per block than the device offers */
+
+/* Bits of the sticky device error word. */
+#define HS_DEVERR_RANGE 1 /* a selected token was >= ctx */
+#define HS_DEVERR_DUP 2   /* a token appeared twice in one selection row */
+#define HS_DEVERR_STATE 4 /* metadata found inconsistent (never set by correct use) */
+
+/*
+ * Geometry and memory of a pool of layers x max_batch request-layers.
+ *   layers, max_batch, ctx, slots, topk_max: >= 1; topk_max <= slots <= 65535 (k selections never exceed the
+ *     fixed-size cache, "HiSparse" paper, Abstract: the GPU cache bounds the decode footprint).
+ *   row_bytes: bytes of one KV row (or page); > 0 and a multiple of 16.
+ *   host_pool: host rows of request b, layer l, token t at
+ *       host_pool + l*host_layer_stride + b*host_req_stride + t*row_bytes.
+ *     Must be page-locked and mapped into the device address space (cudaHostAlloc with cudaHostAllocMapped,
+ *     or hs_host_alloc) and 16-byte aligned. May be NULL when noio_src is given.
+ *   host_layer_stride: bytes between layers; 0 lets every layer read one shared pool (for benchmarks whose
+ *     full history does not fit in host memory). Multiple of 16, >= 0.
+ *   host_req_stride: bytes between requests; 0 means ctx*row_bytes. Multiple of 16.
+ *   hot_buf: device memory [layers][max_batch][slots][row_bytes], 16-byte aligned. Not initialised here.
+ *   meta: device memory of hs_meta_bytes(desc) bytes, 256-byte aligned, holding the metadata arrays, the step
+ *     counter, the counters and the error word. Initialised by hs_pool_create.
+ *   noio_src: optional device copy of the row source with the same strides. When non-NULL, misses are fetched
+ *     from it instead of the host pool ("no-IO" mode, which isolates the cost of resolution from host IO,
+ *     "HiSparse" paper, Abstract: the no-IO oracle).
+ */
+typedef struct {
+  int32_t layers;
+  int32_t max_batch;
+  int32_t ctx;
+  int32_t slots;
+  int32_t topk_max;
+  int32_t row_bytes;
+  const void *host_pool;
+  int64_t host_layer_stride;
+  int64_t host_req_stride;
+  void *hot_buf;
+  void *meta;
+  const void *noio_src;
+} hs_pool_desc;
+
+/* Byte offsets of the arrays inside `meta` (for inspection and checkpointing; the layout is stable):
+ *   step: int32; error: int32; counters: uint64 [layers][4] = (hits, misses, evictions, bytes fetched);
+ *   tok2slot: int32 [layers][max_batch][ctx]; slot_tok, slot_stamp: int32 [layers][max_batch][slots]. */
+typedef struct {
+  size_t step;
+  size_t error;
+  size_t counters;
+  size_t tok2slot;
+  size_t slot_tok;
+  size_t slot_stamp;
+  size_t total;
+} hs_meta_layout;
+
+/* Bytes of device metadata a descriptor needs (0 if the geometry is invalid). */
+size_t hs_meta_bytes(const hs_pool_desc *desc);
+
+/* Fill *out with the metadata layout of a descriptor. HS_ERR_INVALID_ARG on a bad geometry. */
+int hs_get_meta_layout(const hs_pool_desc *desc, hs_meta_layout *out);
+
+/*
+ * Validate the descriptor, bind the pool to the current device, and enqueue on `stream` the initialisation of
+ * the metadata: every cache empty (tok2slot = slot_tok = -1, stamps 0), step 0, counters and error word 0.
+ * *out receives the opaque handle (host memory owned by the library until hs_pool_destroy).
+ */
+int hs_pool_create(const hs_pool_desc *desc, hs_stream_t stream, hs_pool **out);
+
+/* Enqueue the same initialisation again (every cache emptied, step and counters back to 0). Capturable. */
+int hs_pool_reset(hs_pool *pool, hs_stream_t stream);
+
+/* Enqueue "step += 1" on the device step counter; call once per decode step before that step's resolves.
+ * Stamps are decode step numbers, so every layer resolved in one step stamps with the same value. */
+int hs_step_begin(hs_pool *pool, hs_stream_t stream);
+
+/*
+ * Resolve one layer's selections for requests 0..batch-1 (batch row b is pool request b) at the current step:
+ * hit test, LRU victim choice, metadata update and the fetch of every missing row into its hot slot, in one
+ * kernel ("HiSparse" paper, Abstract). topk_idx: device int32 [batch][k], row-major; out_slots: device int32
+ * [batch][k], written in input order. 1 <= batch <= max_batch, 1 <= k <= topk_max; batch == 0 or k == 0 is a
+ * no-op. Enqueued on `stream`.
+ */
+int hs_resolve(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk_idx, int32_t k,
+               int32_t *out_slots, hs_stream_t stream);
+
+/*
+ * Exact layer-wise prefetch for models whose layers share one selection ("HiSparse" paper, Abstract): the same
+ * resolution as hs_resolve for `layer` at the current step, without writing out_slots. A later hs_resolve of
+ * the same layer and selection in the same step finds every token resident, re-stamps the hits with the same
+ * step value and only emits the slots, so prefetch + resolve leaves exactly the state of resolve alone. Run it
+ * on a second stream; calls on different layers touch disjoint state.
+ */
+int hs_prefetch(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk_idx, int32_t k,
+                hs_stream_t stream);
+
+/* Synchronise the device, then read the sticky device error word into *out (HS_DEVERR_* bits); clear it when
+ * `clear` is non-zero. */
+int hs_get_error(hs_pool *pool, int32_t *out, int32_t clear);
+
+/* Synchronise the device, then read layer `layer`'s counters: out[0..3] = hits, misses, evictions, bytes. */
+int hs_get_counters(hs_pool *pool, int32_t layer, uint64_t out[4]);
+
+/* Release the opaque handle. Caller memory is untouched. */
+int hs_pool_destroy(hs_pool *pool);
+
+/* Page-locked, device-mapped, portable host allocation for a host pool (not for the hot path). */
+int hs_host_alloc(size_t bytes, void **out);
+int hs_host_free(void *ptr);
+
+/*
+ * Measure the host link this pool fetches over (not for the hot path; synchronises and creates two events).
+ * Reads `bytes` of the mapped host buffer `host` with the same 16-byte SM loads the resolve kernel uses
+ * (zero-copy, all SMs), and copies them with cudaMemcpyAsync into the device buffer `dev` (>= bytes), each
+ * `iters` times after one warm-up; reports the best of each in GB/s (1e9 bytes/s). bytes: multiple of 16.
+ */
+int hs_probe_link(const void *host, void *dev, size_t bytes, int32_t iters, hs_stream_t stream,
+                  double *zero_copy_gbs, double *memcpy_gbs);
+
+/* Static text for an HS_ERR_* code. */
+const char *hs_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HS_H_ */

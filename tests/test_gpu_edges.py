@@ -1,0 +1,198 @@
+"""Edge cases of the GPU path against the CPU oracle: every cluster size, padding and ragged k, rejected rows,
+empty calls, wide stamp ranges (multi-pass victim sort), long token keys, and host-side argument errors."""
+import numpy as np
+import pytest
+import torch
+
+import hierarchical_sparse_attention_hs_gb300 as hs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+
+    g.build()
+
+
+def _pool(layers, batch, ctx, slots, topk_max, row_bytes, seed=0):
+    buf = hs.PoolBuffers(layers, batch, ctx, slots, topk_max, row_bytes, host_layers=layers)
+    rng = np.random.default_rng(seed)
+    h = buf.host.numpy()
+    h[:] = rng.integers(0, 256, size=h.shape, dtype=np.uint8)
+    buf.create()
+    return buf
+
+
+def _rand_sel(rng, batch, k, ctx, prev=None, keep=0.6, pad=0.0):
+    out = np.empty((batch, k), dtype=np.int32)
+    for b in range(batch):
+        n_keep = int(keep * k) if prev is not None else 0
+        kept = rng.choice(prev[b][prev[b] >= 0], size=min(n_keep, int((prev[b] >= 0).sum())), replace=False) \
+            if prev is not None else np.empty(0, dtype=np.int64)
+        rest = np.setdiff1d(rng.choice(ctx, size=min(ctx, 3 * k), replace=False), kept)[: k - len(kept)]
+        row = np.concatenate([kept, rest]).astype(np.int32)
+        rng.shuffle(row)
+        if pad:
+            row[rng.random(k) < pad] = -1
+        out[b] = row
+    return out
+
+
+def _run(buf, ora, sels, layer=0, set_step=None):
+    stream = torch.cuda.Stream()
+    batch, k = sels[0].shape
+    for sel in sels:
+        with torch.cuda.stream(stream):
+            if set_step is not None:
+                buf.view("step").fill_(set_step)
+            hs.hs_step_begin(buf.handle, stream)
+            t = torch.from_numpy(sel).cuda()
+            out = torch.full((batch, k), -9, dtype=torch.int32, device="cuda")
+            hs.hs_resolve(buf.handle, layer, batch, t, k, out, stream)
+        stream.synchronize()
+        if set_step is not None:
+            ora.step = set_step
+            set_step = None
+        ora.step_begin()
+        expect = ora.resolve(layer, sel, None)
+        assert np.array_equal(out.cpu().numpy(), expect)
+    for name, ref in (("tok2slot", ora.tok2slot), ("slot_tok", ora.slot_tok), ("slot_stamp", ora.slot_stamp)):
+        assert np.array_equal(buf.view(name).cpu().numpy(), ref), name
+    assert np.array_equal(buf.view("counters").cpu().numpy().astype(np.uint64), ora.counters)
+
+
+def _check_rows(buf):
+    host = buf.host.numpy().reshape(buf.layers, buf.max_batch, buf.ctx, buf.row_bytes)
+    st = buf.view("slot_tok").cpu().numpy()
+    hot = buf.hot_view().cpu().numpy()
+    for l in range(buf.layers):
+        for b in range(buf.max_batch):
+            occ = st[l, b] >= 0
+            assert np.array_equal(hot[l, b][occ], host[l, b][st[l, b][occ]])
+            assert not hot[l, b][~occ].any()
+
+
+@pytest.mark.parametrize("batch", [80, 32, 16, 5, 1])  # cluster sizes 1, 2, 4, 8, 8
+def test_every_cluster_size(batch):
+    rng = np.random.default_rng(batch)
+    ctx, slots, k, R = 5000, 300, 120, 48
+    buf = _pool(1, batch, ctx, slots, k, R, seed=batch)
+    ora = oracle.OraclePool(ctx, slots, R, 1, batch, track_rows=False)
+    sels, prev = [], None
+    for s in range(12):
+        prev = _rand_sel(rng, batch, k, ctx, prev, keep=0.0 if s == 6 else 0.6)
+        sels.append(prev)
+    _run(buf, ora, sels)
+    _check_rows(buf)
+    buf.close()
+
+
+def test_padding_and_ragged_k():
+    rng = np.random.default_rng(5)
+    ctx, slots, kmax, R = 3000, 257, 200, 32
+    buf = _pool(2, 6, ctx, slots, kmax, R, seed=5)
+    ora = oracle.OraclePool(ctx, slots, R, 2, 6, track_rows=False)
+    prev = None
+    sels = []
+    for s in range(10):
+        prev = _rand_sel(rng, 6, 77, ctx, prev, keep=0.5, pad=0.15)  # k = 77 < topk_max, 15% padding
+        sels.append(prev)
+    _run(buf, ora, sels, layer=1)
+    _check_rows(buf)
+    buf.close()
+
+
+def test_rejected_rows_change_nothing():
+    rng = np.random.default_rng(9)
+    ctx, slots, k, R = 1000, 64, 16, 16
+    buf = _pool(1, 4, ctx, slots, k, R, seed=9)
+    ora = oracle.OraclePool(ctx, slots, R, 1, 4, track_rows=False)
+    base = _rand_sel(rng, 4, k, ctx)
+    _run(buf, ora, [base])
+    bad = _rand_sel(rng, 4, k, ctx, prev=base, keep=0.5)
+    bad[0, 3] = ctx            # out of range
+    bad[1, 5] = bad[1, 7]      # duplicate
+    hit_tok = base[2, 0]
+    bad[2, :2] = hit_tok       # duplicate of a resident token (caught among hits)
+    _run(buf, ora, [bad])
+    assert ora.error == (oracle.ERR_RANGE | oracle.ERR_DUP)
+    assert hs.hs_get_error(buf.handle, clear=True) == (hs.HS_DEVERR_RANGE | hs.HS_DEVERR_DUP)
+    assert hs.hs_get_error(buf.handle) == 0
+    # row 3 was valid and was resolved normally; the next steps continue in lockstep with the oracle
+    _run(buf, ora, [_rand_sel(rng, 4, k, ctx, prev=base, keep=0.3)])
+    buf.close()
+
+
+def test_empty_calls_are_noops():
+    buf = _pool(1, 2, 100, 8, 4, 16)
+    before = buf.meta.clone()
+    t = torch.zeros((2, 4), dtype=torch.int32, device="cuda")
+    hs.hs_resolve(buf.handle, 0, 0, t, 4, t)
+    hs.hs_resolve(buf.handle, 0, 2, t, 0, t)
+    hs.hs_prefetch(buf.handle, 0, 0, t, 4)
+    torch.cuda.synchronize()
+    assert torch.equal(before, buf.meta)
+    buf.close()
+
+
+def test_wide_stamp_range_multi_pass_victim_sort():
+    # jump the step counter so stamps span > 2^16: the victim sort needs three 8-bit passes
+    rng = np.random.default_rng(11)
+    ctx, slots, k, R = 4000, 200, 40, 16
+    buf = _pool(1, 3, ctx, slots, k, R, seed=11)
+    ora = oracle.OraclePool(ctx, slots, R, 1, 3, track_rows=False)
+    prev = None
+    first = []
+    for s in range(6):
+        prev = _rand_sel(rng, 3, k, ctx, prev, keep=0.2)
+        first.append(prev)
+    _run(buf, ora, first)
+    later = []
+    for s in range(8):
+        prev = _rand_sel(rng, 3, k, ctx, prev, keep=0.5)
+        later.append(prev)
+    _run(buf, ora, later, set_step=70000)
+    assert int(buf.view("slot_stamp").max()) > 70000 and int(buf.view("slot_stamp")[buf.view("slot_stamp") > 0].min()) < 10
+    _check_rows(buf)
+    buf.close()
+
+
+def test_long_token_keys():
+    # ctx = 2^23: token keys need three 8-bit passes, the top pass nearly empty
+    rng = np.random.default_rng(13)
+    ctx, slots, k, R = 1 << 23, 96, 64, 16
+    buf = _pool(1, 2, ctx, slots, k, R, seed=13)
+    ora = oracle.OraclePool(ctx, slots, R, 1, 2, track_rows=False)
+    prev = None
+    sels = []
+    for s in range(8):
+        prev = _rand_sel(rng, 2, k, ctx, prev, keep=0.4)
+        sels.append(prev)
+    _run(buf, ora, sels)
+    _check_rows(buf)
+    buf.close()
+
+
+def test_argument_errors():
+    buf = _pool(2, 4, 100, 16, 8, 16)
+    t = torch.zeros((4, 8), dtype=torch.int32, device="cuda")
+    for args in [(2, 4, t, 8, t), (-1, 4, t, 8, t), (0, 5, t, 8, t), (0, 4, t, 9, t), (0, 4, None, 8, t),
+                 (0, 4, t, 8, None)]:
+        with pytest.raises(hs.HsError) as e:
+            hs.hs_resolve(buf.handle, *args)
+        assert e.value.code == hs.HS_ERR_INVALID_ARG
+    # a host pool that is not page-locked mapped memory is refused
+    plain = np.zeros(2 * 4 * 100 * 16, dtype=np.uint8)
+    d = hs.hs_pool_desc(2, 4, 100, 16, 8, 16, plain.ctypes.data, 0, 0, buf.hot.data_ptr(), buf.meta.data_ptr(), None)
+    with pytest.raises(hs.HsError) as e:
+        hs.hs_pool_create(d)
+    assert e.value.code == hs.HS_ERR_NOT_MAPPED
+    # misaligned meta
+    d = hs.hs_pool_desc(2, 4, 100, 16, 8, 16, buf.host.ptr, 0, 0, buf.hot.data_ptr(), buf.meta.data_ptr() + 16, None)
+    with pytest.raises(hs.HsError) as e:
+        hs.hs_pool_create(d)
+    assert e.value.code == hs.HS_ERR_INVALID_ARG
+    buf.close()

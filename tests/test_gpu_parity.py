@@ -1,0 +1,71 @@
+"""GPU path (through the C ABI) against the CPU oracle, bit for bit: out_slots after every call, the whole
+metadata state (tok2slot, slot_tok, slot_stamp, counters) and every hot-buffer byte, on all five workloads at
+their full sizes, in the launch configuration the benchmark uses."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as gh
+import workload as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+
+    g.build()
+
+
+def test_tiny_full_state_and_rows():
+    import oracle
+
+    w = wl.WORKLOADS["tiny"]
+    buf, ora = gh.replay(w)
+    # the oracle with rows tracked: compare every hot-buffer byte directly
+    ora2 = oracle.OraclePool(w.ctx, w.slots, w.row_bytes, 1, 1, track_rows=True)
+    sel = wl.gen_selections(w)
+    host = gh.host_rows(buf)[0]
+    for s in range(w.steps):
+        ora2.step_begin()
+        ora2.resolve(0, sel[s, 0], host)
+    assert np.array_equal(buf.hot_view().cpu().numpy(), ora2.hot)
+    buf.close()
+
+
+@pytest.mark.parametrize("name", ["dsa", "multilayer", "quest", "shared"])
+def test_workload_parity(name):
+    w = wl.WORKLOADS[name]
+    buf, ora = gh.replay(w)
+    gh.check_hot_rows(buf)
+    buf.close()
+
+
+def test_dsa_graph_replay_matches_oracle():
+    w = wl.WORKLOADS["dsa"]
+    buf, _ = gh.replay(w, steps=24, graphs=True)
+    gh.check_hot_rows(buf)
+    buf.close()
+
+
+def test_dsa_noio_mode():
+    w = wl.WORKLOADS["dsa"]
+    buf, _ = gh.replay(w, steps=20, noio=True)
+    gh.check_hot_rows(buf)
+    buf.close()
+
+
+def test_shared_with_layerwise_prefetch_is_exact():
+    # prefetch(l+1) on a second stream + resolve(l): the state must equal a lone resolve's (the oracle's)
+    w = wl.WORKLOADS["shared"]
+    buf, _ = gh.replay(w, steps=8, prefetch=True)
+    gh.check_hot_rows(buf)
+    buf.close()
+
+
+def test_shared_prefetch_in_graph():
+    w = wl.WORKLOADS["shared"]
+    buf, _ = gh.replay(w, steps=4, prefetch=True, graphs=True)
+    gh.check_hot_rows(buf, layers=[0, 1, 77])
+    buf.close()
