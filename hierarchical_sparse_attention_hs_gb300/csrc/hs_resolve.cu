@@ -60,14 +60,20 @@ struct ResolveArgs {
   int32_t cluster;          // CTAs per request-layer
 };
 
+// Contexts up to this many selection units rank their misses with a shared-memory bitmap (one bit per unit plus
+// a 16-bit running count per 32 units); longer contexts use the radix sort.
+constexpr int BITMAP_MAX_CTX = 1 << 18;
+
 // Shared-memory carve-up, identical on host and device.
 struct SmemLayout {
-  size_t sel, slot, stamp, stok, hit, midx, cidx, tbl, red, total;
+  size_t sel, slot, stamp, stok, hit, mpos, rank, cidx, mscr, tbl, red, total;
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-__host__ __device__ inline SmemLayout smem_layout(int k, int slots) {
+__host__ __device__ inline bool use_bitmap(int ctx) { return ctx <= BITMAP_MAX_CTX; }
+
+__host__ __device__ inline SmemLayout smem_layout(int k, int slots, int ctx) {
   SmemLayout L;
   size_t o = 0;
   L.sel = o;   o = align16(o + sizeof(int32_t) * k);
@@ -75,8 +81,17 @@ __host__ __device__ inline SmemLayout smem_layout(int k, int slots) {
   L.stamp = o; o = align16(o + sizeof(int32_t) * slots);
   L.stok = o;  o = align16(o + sizeof(int32_t) * slots);
   L.hit = o;   o = align16(o + sizeof(uint32_t) * ((slots + 31) / 32));
-  L.midx = o;  o = align16(o + sizeof(uint16_t) * 2 * k);
+  L.mpos = o;  o = align16(o + sizeof(uint16_t) * k);
+  L.rank = o;  o = align16(o + sizeof(uint16_t) * k);
   L.cidx = o;  o = align16(o + sizeof(uint16_t) * 2 * slots);
+  L.mscr = o;
+  if (use_bitmap(ctx)) {
+    const size_t words = ((size_t)ctx + 31) / 32;
+    o = align16(o + sizeof(uint32_t) * words);
+    o = align16(o + sizeof(uint16_t) * words);
+  } else {
+    o = align16(o + sizeof(uint16_t) * 2 * k);
+  }
   L.tbl = o;   o = align16(o + sizeof(int32_t) * NW * TBL_STRIDE);
   L.red = o;   o = align16(o + sizeof(int32_t) * 4 * (NW + 1));
   L.total = o;
@@ -241,6 +256,90 @@ __device__ uint16_t* radix_sort(int n, int key_bits, uint16_t* buf0, uint16_t* b
   return cur;
 }
 
+// Order-preserving compaction of the indices i in [0, n) with pred(i) into out; returns the count (same on all
+// threads). Each warp owns a contiguous segment; a ballot gives the in-warp offsets.
+template <class Pred>
+__device__ int block_compact(int n, uint16_t* __restrict__ out, Pred pred, int* __restrict__ red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = (n + NW - 1) / NW;
+  const int beg = min(n, warp * seg);
+  const int end = min(n, beg + seg);
+  int c = 0;
+  for (int i = beg + lane; i < end; i += 32) c += pred(i) ? 1 : 0;
+  c = __reduce_add_sync(0xffffffffu, c);
+  if (lane == 0) red[warp] = c;
+  __syncthreads();
+  int run = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    const int x = red[w];
+    run += w < warp ? x : 0;
+    total += x;
+  }
+  __syncthreads();
+  for (int base = beg; base < end; base += 32) {
+    const int i = base + lane;
+    const bool f = i < end && pred(i);
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    if (f) out[run + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)i;
+    run += __popc(bal);
+  }
+  __syncthreads();
+  return total;
+}
+
+// Rank of every miss among the misses by token, with a bitmap over the context: rank(t) = number of set bits
+// below t = running count of the word holding t + popcount of its lower bits. Also flags a token set twice.
+// mpos: miss positions (m of them); sel: selection row; rank_of_pos[pos] receives the rank.
+__device__ unsigned bitmap_ranks(int m, int ctx, const uint16_t* __restrict__ mpos, const int32_t* __restrict__ sel,
+                                 uint16_t* __restrict__ rank_of_pos, uint32_t* __restrict__ bits,
+                                 uint16_t* __restrict__ prefix, int* __restrict__ red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwords = (ctx + 31) >> 5;
+  unsigned bad = 0;
+  for (int w = threadIdx.x; w < nwords; w += NT) bits[w] = 0u;
+  __syncthreads();
+  for (int q = threadIdx.x; q < m; q += NT) {
+    const int t = sel[mpos[q]];
+    const uint32_t bit = 1u << (t & 31);
+    if (atomicOr(&bits[t >> 5], bit) & bit) bad |= HS_DEVERR_DUP;
+  }
+  __syncthreads();
+  const int seg = (nwords + NW - 1) / NW;
+  const int beg = min(nwords, warp * seg);
+  const int end = min(nwords, beg + seg);
+  int c = 0;
+  for (int w = beg + lane; w < end; w += 32) c += __popc(bits[w]);
+  c = __reduce_add_sync(0xffffffffu, c);
+  if (lane == 0) red[warp] = c;
+  __syncthreads();
+  int run = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) run += w < warp ? red[w] : 0;
+  __syncthreads();
+  for (int base = beg; base < end; base += 32) {
+    const int w = base + lane;
+    const int p = w < end ? __popc(bits[w]) : 0;
+    int incl = p;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (w < end) prefix[w] = (uint16_t)(run + incl - p);
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncthreads();
+  for (int q = threadIdx.x; q < m; q += NT) {
+    const int pos = mpos[q];
+    const int t = sel[pos];
+    const int w = t >> 5;
+    rank_of_pos[pos] = (uint16_t)(prefix[w] + __popc(bits[w] & ((1u << (t & 31)) - 1u)));
+  }
+  __syncthreads();
+  return bad;
+}
+
 __device__ __forceinline__ int bits_of(unsigned x) { return x ? 32 - __clz(x) : 0; }
 
 __device__ __forceinline__ uint4 load_row_chunk_host(const uint8_t* p) {
@@ -259,16 +358,23 @@ __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 template <bool FROM_HOST>
+__device__ __forceinline__ uint4 load_row_chunk(const uint8_t* p) {
+  return FROM_HOST ? load_row_chunk_host(p) : load_row_chunk_device(p);
+}
+
+template <bool FROM_HOST, bool BITMAP>
 __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const SmemLayout L = smem_layout(a.k, a.slots);
+  const SmemLayout L = smem_layout(a.k, a.slots, a.ctx);
   int32_t* s_sel = reinterpret_cast<int32_t*>(smem + L.sel);
   int32_t* s_slot = reinterpret_cast<int32_t*>(smem + L.slot);
   int32_t* s_stamp = reinterpret_cast<int32_t*>(smem + L.stamp);
   int32_t* s_stok = reinterpret_cast<int32_t*>(smem + L.stok);
   uint32_t* s_hit = reinterpret_cast<uint32_t*>(smem + L.hit);
-  uint16_t* s_midx = reinterpret_cast<uint16_t*>(smem + L.midx);
+  uint16_t* s_mpos = reinterpret_cast<uint16_t*>(smem + L.mpos);
+  uint16_t* s_rank = reinterpret_cast<uint16_t*>(smem + L.rank);
   uint16_t* s_cidx = reinterpret_cast<uint16_t*>(smem + L.cidx);
+  uint8_t* s_mscr = smem + L.mscr;
   int* s_tbl = reinterpret_cast<int*>(smem + L.tbl);
   int* s_red = reinterpret_cast<int*>(smem + L.red);
 
@@ -281,13 +387,15 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   const int rank = blockIdx.x % C;
   const int b = blockIdx.x / C;
   const int tid = threadIdx.x;
-  const int k = a.k, H = a.slots, ctx = a.ctx;
+  const int k = a.k, H = a.slots, ctx = a.ctx, R = a.row_bytes;
   const int32_t step = __ldcg(a.step);
   int32_t* t2s = a.tok2slot + (size_t)b * ctx;
   int32_t* s2t = a.slot_tok + (size_t)b * H;
   int32_t* stp = a.slot_stamp + (size_t)b * H;
   const int32_t* sel = a.topk + (size_t)b * k;
   int32_t* out = a.out_slots ? a.out_slots + (size_t)b * k : nullptr;
+  const uint8_t* src = a.src + (size_t)b * (size_t)a.src_req_stride;
+  uint8_t* hot = a.hot + (size_t)b * (size_t)H * (size_t)R;
 
   // 1. selection row, slot metadata, empty hit bitmap
   unsigned bad = 0;
@@ -304,7 +412,6 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   __syncthreads();
 
   // 2. hit test
-  int nhit = 0;
   for (int i = tid; i < k; i += NT) {
     const int32_t t = s_sel[i];
     int32_t s = (t >= 0 && t < ctx) ? __ldcg(t2s + t) : -1;
@@ -316,24 +423,53 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     if (s >= 0) {
       const uint32_t bit = 1u << (s & 31);
       if (atomicOr(&s_hit[s >> 5], bit) & bit) bad |= HS_DEVERR_DUP;
-      ++nhit;
     }
   }
   __syncthreads();
   // Every read of the cluster-shared metadata by this CTA has completed.
   if (C > 1) cluster_arrive();
-  nhit = block_sum(nhit, s_red);
 
-  // 3. misses sorted by token (filter fused into the first pass)
-  int m = 0;
-  const int tok_bits = bits_of((unsigned)(ctx - 1));
-  const uint16_t* midx = radix_sort(
-      k, tok_bits, s_midx, s_midx + k, [&](int i) { return s_sel[i]; },
-      [&](int i) { return s_slot[i] < 0 && s_sel[i] >= 0 && s_sel[i] < ctx; }, s_tbl, s_red, &m);
-  for (int j = tid + 1; j < m; j += NT)
-    if (s_sel[midx[j]] == s_sel[midx[j - 1]]) bad |= HS_DEVERR_DUP;
+  // 3. misses in selection order
+  auto is_miss = [&](int i) { return s_slot[i] < 0 && s_sel[i] >= 0 && s_sel[i] < ctx; };
+  const int m = block_compact(k, s_mpos, is_miss, s_red);
 
-  // 4. victims: non-selected slots by (stamp, slot)
+  // 4. start this CTA's first wave of row loads now, so the host link is busy while the ranks and victims are
+  //    being worked out; chunk c is 16-byte chunk (c % cpr) of the (c / cpr)-th miss in selection order
+  const int cpr = R >> 4;
+  const long long nchunk = (long long)m * cpr;
+  const long long stride = (long long)C * NT;
+  const long long c_first = (long long)rank * NT + tid;
+  uint4 pre[COPY_UNROLL];
+#pragma unroll
+  for (int u = 0; u < COPY_UNROLL; ++u) {
+    const long long c = c_first + u * stride;
+    if (c < nchunk) {
+      const int q = (int)(c / cpr);
+      const int w = (int)(c - (long long)q * cpr);
+      pre[u] = load_row_chunk<FROM_HOST>(src + (size_t)s_sel[s_mpos[q]] * (size_t)R + ((size_t)w << 4));
+    }
+  }
+
+  // 5. rank of each miss among the misses by token
+  if (BITMAP) {
+    uint32_t* bits = reinterpret_cast<uint32_t*>(s_mscr);
+    uint16_t* prefix = reinterpret_cast<uint16_t*>(s_mscr + align16(sizeof(uint32_t) * (size_t)((ctx + 31) >> 5)));
+    bad |= bitmap_ranks(m, ctx, s_mpos, s_sel, s_rank, bits, prefix, s_red);
+  } else {
+    uint16_t* mbuf = reinterpret_cast<uint16_t*>(s_mscr);
+    int m2 = 0;
+    const uint16_t* midx = radix_sort(
+        m, bits_of((unsigned)(ctx - 1)), mbuf, mbuf + k, [&](int q) { return s_sel[s_mpos[q]]; },
+        [](int) { return true; }, s_tbl, s_red, &m2);
+    for (int j = tid; j < m; j += NT) {
+      const int pos = s_mpos[midx[j]];
+      s_rank[pos] = (uint16_t)j;
+      if (j && s_sel[pos] == s_sel[s_mpos[midx[j - 1]]]) bad |= HS_DEVERR_DUP;
+    }
+    __syncthreads();
+  }
+
+  // 6. victims: non-selected slots by (stamp, slot)
   int lo = 0x7fffffff, hi = -1;
   for (int v = tid; v < H; v += NT) {
     if (!(s_hit[v >> 5] & (1u << (v & 31)))) {
@@ -360,18 +496,18 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     return;
   }
 
-  // 5a. hits: stamp and emit
+  // 7a. hits: stamp and emit
   for (int i = rank * NT + tid; i < k; i += C * NT) {
     const int32_t s = s_slot[i];
     if (s >= 0) stp[s] = step;
     if (out && (s >= 0 || s_sel[i] < 0)) out[i] = s;
   }
-  // 5b. misses: the j-th smallest token takes the j-th victim
+  // 7b. misses: the j-th smallest token takes the j-th victim
   int nevict = 0;
-  for (int j = rank * NT + tid; j < m; j += C * NT) {
-    const int pos = midx[j];
+  for (int q = rank * NT + tid; q < m; q += C * NT) {
+    const int pos = s_mpos[q];
     const int32_t t = s_sel[pos];
-    const int32_t v = cidx[j];
+    const int32_t v = cidx[s_rank[pos]];
     const int32_t u = s_stok[v];
     if (u >= 0) {
       t2s[u] = -1;
@@ -382,23 +518,19 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     stp[v] = step;
     if (out) out[pos] = v;
   }
-  nevict = block_sum(nevict, s_red);
-  if (tid == 0) {
-    if (nevict) atomicAdd(a.counters + 2, (unsigned long long)nevict);
-    if (rank == 0) {
-      atomicAdd(a.counters + 0, (unsigned long long)nhit);
-      atomicAdd(a.counters + 1, (unsigned long long)m);
-      atomicAdd(a.counters + 3, (unsigned long long)m * (unsigned long long)a.row_bytes);
+  // 7c. the first wave of rows lands in its slots
+#pragma unroll
+  for (int u = 0; u < COPY_UNROLL; ++u) {
+    const long long c = c_first + u * stride;
+    if (c < nchunk) {
+      const int q = (int)(c / cpr);
+      const int w = (int)(c - (long long)q * cpr);
+      const size_t v = cidx[s_rank[s_mpos[q]]];
+      *reinterpret_cast<uint4*>(hot + v * (size_t)R + ((size_t)w << 4)) = pre[u];
     }
   }
-
-  // 5c. row copies: chunk c of the m*cpr 16-byte chunks is chunk (c % cpr) of miss c / cpr
-  const int cpr = a.row_bytes >> 4;
-  const long long nchunk = (long long)m * cpr;
-  const uint8_t* src = a.src + (size_t)b * (size_t)a.src_req_stride;
-  uint8_t* hot = a.hot + (size_t)b * (size_t)H * (size_t)a.row_bytes;
-  const long long stride = (long long)C * NT;
-  for (long long c0 = (long long)rank * NT + tid; c0 < nchunk; c0 += stride * COPY_UNROLL) {
+  // 7d. the remaining rows, COPY_UNROLL loads in flight per thread
+  for (long long c0 = c_first + stride * COPY_UNROLL; c0 < nchunk; c0 += stride * COPY_UNROLL) {
     uint4 v[COPY_UNROLL];
     uint8_t* dst[COPY_UNROLL];
 #pragma unroll
@@ -406,18 +538,28 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
       const long long c = c0 + u * stride;
       dst[u] = nullptr;
       if (c < nchunk) {
-        const int j = (int)(c / cpr);
-        const int w = (int)(c - (long long)j * cpr);
-        const size_t t = (size_t)s_sel[midx[j]];
-        const size_t slot = (size_t)cidx[j];
-        const uint8_t* p = src + t * (size_t)a.row_bytes + ((size_t)w << 4);
-        v[u] = FROM_HOST ? load_row_chunk_host(p) : load_row_chunk_device(p);
-        dst[u] = hot + slot * (size_t)a.row_bytes + ((size_t)w << 4);
+        const int q = (int)(c / cpr);
+        const int w = (int)(c - (long long)q * cpr);
+        const int pos = s_mpos[q];
+        v[u] = load_row_chunk<FROM_HOST>(src + (size_t)s_sel[pos] * (size_t)R + ((size_t)w << 4));
+        dst[u] = hot + (size_t)cidx[s_rank[pos]] * (size_t)R + ((size_t)w << 4);
       }
     }
 #pragma unroll
     for (int u = 0; u < COPY_UNROLL; ++u)
       if (dst[u]) *reinterpret_cast<uint4*>(dst[u]) = v[u];
+  }
+  nevict = block_sum(nevict, s_red);
+  int nvalid = 0;
+  for (int i = tid; i < k; i += NT) nvalid += s_sel[i] >= 0 ? 1 : 0;
+  nvalid = block_sum(nvalid, s_red);
+  if (tid == 0) {
+    if (nevict) atomicAdd(a.counters + 2, (unsigned long long)nevict);
+    if (rank == 0) {
+      atomicAdd(a.counters + 0, (unsigned long long)(nvalid - m));
+      atomicAdd(a.counters + 1, (unsigned long long)m);
+      atomicAdd(a.counters + 3, (unsigned long long)m * (unsigned long long)R);
+    }
   }
 }
 
@@ -503,6 +645,24 @@ bool layout_of(const hs_pool_desc* d, hs_meta_layout* L) {
   return true;
 }
 
+// Device-visible address of page-locked (cudaHostAlloc / cudaHostRegister) host memory, or nullptr. Plain
+// pageable memory is refused even where the GPU could reach it through the CPU's page tables: the host tier
+// must stay resident while kernels read it.
+const void* mapped_host_ptr(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost) return nullptr;
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, const_cast<void*>(p), 0) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return d;
+}
+
 bool is_device_ptr(const void* p) {
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
@@ -563,7 +723,7 @@ int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3((unsigned)(batch * a.cluster), 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = smem_layout(k, p->d.slots).total;
+  cfg.dynamicSmemBytes = smem_layout(k, p->d.slots, p->d.ctx).total;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;
@@ -579,8 +739,14 @@ int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk
   }
   cfg.attrs = attr;
   cfg.numAttrs = (unsigned)na;
-  const cudaError_t e = p->noio ? cudaLaunchKernelEx(&cfg, hs_resolve_kernel<false>, a)
-                                : cudaLaunchKernelEx(&cfg, hs_resolve_kernel<true>, a);
+  const bool bm = use_bitmap(p->d.ctx);
+  cudaError_t e;
+  if (p->noio)
+    e = bm ? cudaLaunchKernelEx(&cfg, hs_resolve_kernel<false, true>, a)
+           : cudaLaunchKernelEx(&cfg, hs_resolve_kernel<false, false>, a);
+  else
+    e = bm ? cudaLaunchKernelEx(&cfg, hs_resolve_kernel<true, true>, a)
+           : cudaLaunchKernelEx(&cfg, hs_resolve_kernel<true, false>, a);
   return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 
@@ -614,11 +780,8 @@ int hs_pool_create(const hs_pool_desc* desc, hs_stream_t stream, hs_pool** out) 
     src = static_cast<const uint8_t*>(desc->noio_src);
   } else {
     if (!desc->host_pool || (reinterpret_cast<uintptr_t>(desc->host_pool) & 15)) return HS_ERR_INVALID_ARG;
-    void* dptr = nullptr;
-    if (cudaHostGetDevicePointer(&dptr, const_cast<void*>(desc->host_pool), 0) != cudaSuccess || !dptr) {
-      cudaGetLastError();
-      return HS_ERR_NOT_MAPPED;
-    }
+    const void* dptr = mapped_host_ptr(desc->host_pool);
+    if (!dptr) return HS_ERR_NOT_MAPPED;
     src = static_cast<const uint8_t*>(dptr);
   }
   int dev = 0, sms = 0, optin = 0;
@@ -626,11 +789,15 @@ int hs_pool_create(const hs_pool_desc* desc, hs_stream_t stream, hs_pool** out) 
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return HS_ERR_CUDA;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return HS_ERR_CUDA;
-  const size_t smem = smem_layout(desc->topk_max, desc->slots).total;
+  const size_t smem = smem_layout(desc->topk_max, desc->slots, desc->ctx).total;
   if (smem > (size_t)optin) return HS_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(hs_resolve_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+  if (cudaFuncSetAttribute(hs_resolve_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
           cudaSuccess ||
-      cudaFuncSetAttribute(hs_resolve_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+      cudaFuncSetAttribute(hs_resolve_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(hs_resolve_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(hs_resolve_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
           cudaSuccess)
     return HS_ERR_CUDA;
 
@@ -666,7 +833,7 @@ int hs_pool_create(const hs_pool_desc* desc, hs_stream_t stream, hs_pool** out) 
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, hs_resolve_kernel<true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, hs_resolve_kernel<true, true>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       break;
     }
@@ -758,11 +925,8 @@ int hs_probe_link(const void* host, void* dev, size_t bytes, int32_t iters, hs_s
   if (!host || !dev || bytes < 16 || (bytes & 15) || iters < 1 || !zero_copy_gbs || !memcpy_gbs ||
       (reinterpret_cast<uintptr_t>(host) & 15))
     return HS_ERR_INVALID_ARG;
-  void* dhost = nullptr;
-  if (cudaHostGetDevicePointer(&dhost, const_cast<void*>(host), 0) != cudaSuccess || !dhost) {
-    cudaGetLastError();
-    return HS_ERR_NOT_MAPPED;
-  }
+  const void* dhost = mapped_host_ptr(host);
+  if (!dhost) return HS_ERR_NOT_MAPPED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int dev_id = 0, sms = 0;
   if (cudaGetDevice(&dev_id) != cudaSuccess ||

@@ -155,7 +155,8 @@ int hs_prefetch(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk
  * `clear` is non-zero. */
 int hs_get_error(hs_pool *pool, int32_t *out, int32_t clear);
 
-/* Synchronise the device, then read layer `layer`'s counters: out[0..3] = hits, misses, evictions, bytes. */
+/* Synchronise the device, then read layer `layer`'s counters: out[0..3] = hits, misses, evictions, bytes.
+ * Every call counts: a resolve that follows a prefetch of the same selection adds its k lookups as hits. */
 int hs_get_counters(hs_pool *pool, int32_t layer, uint64_t out[4]);
 
 /* Release the opaque handle. Caller memory is untouched. */

@@ -110,6 +110,11 @@ def replay(w: wl.Workload, steps: int | None = None, host_layers: int = 1, noio:
                 enqueue(s)
         s0.synchronize()
         ora.step_begin()
+        if prefetch:
+            # the oracle makes the same calls: counters count every call, so a resolve after a prefetch adds
+            # its (all-hit) lookups; the state equals a lone resolve's (pinned on the CPU)
+            for l in range(1, L):
+                ora.resolve(l, sel[s, lsel(l)], None, want_slots=False)
         for l in range(L):
             expect = ora.resolve(l, sel[s, lsel(l)], None)
             got = out[l].cpu().numpy()

@@ -39,3 +39,39 @@ def test_invariants_hold_after_every_call(name, layers, reqs, steps):
             misses = int(np.count_nonzero(~np.isin(valid, before[b][0])))
             pins.check_invariants(pool, 0, b, sel[s, 0, b], out[b], host[b], pool.step, before[b], misses)
     assert pool.error == 0
+
+
+@pytest.mark.parametrize("same", [True, False])
+def test_prefetch_then_resolve_equals_resolve_alone(same):
+    """Exact layer-wise prefetch (HiSparse paper, Abstract): prefetch(l) then resolve(l) in the same step leaves
+    the state and out_slots of a lone resolve(l). With a different selection in the resolve (same=False) the
+    second call is an ordinary resolve at the same step, which the brute-force pin covers; here it only has
+    to keep the invariants."""
+    w = wl.WORKLOADS["shared"]
+    sel = wl.gen_selections(w, requests=(0, 2), steps=6)[:, 0]
+    other = wl.gen_selections(wl.WORKLOADS["dsa"], requests=(0, 2), steps=6)[:, 0] % w.ctx
+    host = np.stack([wl.rows(w, 0, b) for b in range(2)])
+    lone = oracle.OraclePool(w.ctx, w.slots, w.row_bytes, 1, 2)
+    pre = oracle.OraclePool(w.ctx, w.slots, w.row_bytes, 1, 2)
+    for s in range(6):
+        lone.step_begin()
+        pre.step_begin()
+        target = sel[s] if same else other[s]
+        out_lone = lone.resolve(0, target, host)
+        assert pre.resolve(0, sel[s], host, want_slots=False) is None
+        before = [(pre.slot_tok[0, b].copy(), pre.hot[0, b].copy()) for b in range(2)]
+        m0 = pre.counters[0, 1]
+        out_pre = pre.resolve(0, target, host)
+        if same:
+            assert pre.counters[0, 1] == m0  # everything was resident
+            assert np.array_equal(out_pre, out_lone)
+            for name in ("tok2slot", "slot_tok", "slot_stamp", "hot"):
+                assert np.array_equal(getattr(pre, name), getattr(lone, name)), name
+        else:
+            for b in range(2):
+                valid = target[b][target[b] >= 0]
+                misses = int(np.count_nonzero(~np.isin(valid, before[b][0])))
+                pins.check_invariants(pre, 0, b, target[b], out_pre[b], host[b], pre.step, before[b], misses)
+        if same:
+            lone_hits = lone.counters[0, 0]
+            assert pre.counters[0, 0] == lone_hits + (s + 1) * 2 * w.topk
