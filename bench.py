@@ -125,6 +125,32 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def kernel_sources_sha16() -> str:
+    import hashlib
+
+    from hierarchical_sparse_attention_hs_gb300 import build as hs_build
+
+    parts = [hashlib.sha256(open(f, "rb").read()).hexdigest() for f in
+             [p for p in hs_build.SOURCES] + [hs_build.HEADERS[1]]]
+    return hashlib.sha256("".join(parts).encode()).hexdigest()[:16]
+
+
+def captured_traffic(w: wl.Workload, cold_launches: int, steady_launches: int):
+    """DRAM bytes per launch from the committed ncu capture of this workload, when the kernel sources are the
+    ones it was taken on; else None."""
+    path = os.path.join(ROOT, "profiles", f"hs_resolve_kernel_{w.name}_ncu.json")
+    try:
+        with open(path) as f:
+            cap = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if cap.get("kernel_sources_sha16") != kernel_sources_sha16():
+        return None
+    d = cap["dram_bytes_per_launch"]
+    n = cold_launches + steady_launches
+    return (cold_launches * d["cold"] + steady_launches * d["steady"]) / n if n else None
+
+
 def meta_bytes_per_launch(w: wl.Workload, batch: int) -> int:
     """Metadata bytes of one resolve launch that do not depend on hits/misses: selection read, tok2slot gather,
     out_slots write (4k each) and the stamp + slot-token reads (8H), per request-layer."""
@@ -158,28 +184,36 @@ class GpuRun:
         self.side = torch.cuda.Stream() if prefetch else None
         self.flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
         torch.cuda.synchronize()
+        try:
+            torch.cuda.Event(enable_timing=True, external=True)
+            self.inner_events = True
+        except TypeError:
+            self.inner_events = False
+        self.mid_events = []
+        self.begin_graph = None
+        if not self.inner_events:
+            self.begin_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.begin_graph, stream=self.stream):
+                hs.hs_step_begin(self.pool, self.stream)
         self.graphs = [self._capture(s) for s in range(w.steps)]
         torch.cuda.synchronize()
 
     def _lsel(self, l):
         return 0 if self.w.shared_across_layers else l
 
-    def enqueue(self, s, topk=None, events=None):
-        """Enqueue decode step s on self.stream (topk: device selections [Lsel][B][k] to use instead of the
-        pre-staged ones). events: optional list receiving (start, end) CUDA events around each resolve launch."""
+    def enqueue(self, s):
+        """Enqueue decode step s on self.stream: hs_step_begin, then the step's resolves."""
+        self.hs.hs_step_begin(self.pool, self.stream)
+        self.enqueue_resolves(s)
+
+    def enqueue_resolves(self, s):
+        """Enqueue the resolves of decode step s (all layers, all requests) on self.stream."""
         torch, hs, w = self.torch, self.hs, self.w
         st = self.stream
-        src = self.sel[s] if topk is None else topk
-        hs.hs_step_begin(self.pool, st)
+        src = self.sel[s]
         if not self.prefetch:
             for l in range(w.layers):
-                if events is not None:
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record(st)
                 hs.hs_resolve(self.pool, l, w.requests, src[self._lsel(l)], w.topk, self.out[l], st)
-                if events is not None:
-                    e1.record(st)
-                    events.append((e0, e1))
             return
         # exact layer-wise prefetch: layer l+1 resolves on the side stream while layer l resolves here
         side = self.side
@@ -200,9 +234,20 @@ class GpuRun:
         st.wait_event(evj)
 
     def _capture(self, s):
-        g = self.torch.cuda.CUDAGraph()
-        with self.torch.cuda.graph(g, stream=self.stream):
-            self.enqueue(s)
+        """One graph per decode step. Where events can be recorded inside a graph, the graph also records a
+        timing event between hs_step_begin and the resolves; otherwise hs_step_begin gets a graph of its own."""
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        if self.inner_events:
+            mid = torch.cuda.Event(enable_timing=True, external=True)
+            with torch.cuda.graph(g, stream=self.stream):
+                self.hs.hs_step_begin(self.pool, self.stream)
+                mid.record(self.stream)
+                self.enqueue_resolves(s)
+            self.mid_events.append(mid)
+        else:
+            with torch.cuda.graph(g, stream=self.stream):
+                self.enqueue_resolves(s)
         return g
 
     def launches_per_step(self) -> int:
@@ -215,50 +260,49 @@ class GpuRun:
     def reset(self):
         self.hs.hs_pool_reset(self.pool, self.stream)
 
-    def run_steps(self, k_steps: int, start: int = 0, timed: bool = True):
-        """Replay k_steps decode steps starting at sequence position `start`; returns per-step ms (or [])."""
+    def run_steps(self, k_steps: int, timed: bool = True):
+        """Replay k_steps decode steps of the sequence from the cold start (the pool must have just been reset),
+        resetting it whenever the sequence wraps (outside the timed intervals). Returns a list of
+        (sequence position, step ms, resolve ms) and the counters (hits, misses, evictions, bytes) summed over
+        layers and steps. The resolve time runs from the end of hs_step_begin to the end of the step."""
         torch = self.torch
-        times = []
-        pos = start
-        for _ in range(k_steps):
-            if pos == self.w.steps:
-                pos = 0
-                self.reset()
-            self.flush()
-            if timed:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(self.stream)
-            with torch.cuda.stream(self.stream):
-                self.graphs[pos].replay()
-            if timed:
-                e1.record(self.stream)
-                times.append((pos, e0, e1))
-            pos += 1
-        self.stream.synchronize()
-        return [(p, a.elapsed_time(b)) for p, a, b in times], pos
-
-    def kernel_pass(self, k_steps: int):
-        """Eager replay of the same steps with events around every hs_resolve launch. Returns (sum of kernel ms,
-        number of launches, counters (hits, misses, evictions, bytes) summed over layers and over the steps)."""
-        torch = self.torch
-        self.reset()
-        evs = []
+        rows, pending = [], []
         totals = np.zeros(4, dtype=np.int64)
+
+        def collect():
+            self.stream.synchronize()
+            for p, e0, em, e1 in pending:
+                rows.append((p, e0.elapsed_time(e1), em.elapsed_time(e1)))
+            pending.clear()
+
         pos = 0
         for _ in range(k_steps):
             if pos == self.w.steps:
-                pos = 0
-                self.stream.synchronize()
+                collect()
                 totals += self.counters_total()
+                pos = 0
                 self.reset()
             self.flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(self.stream):
-                self.enqueue(pos, events=evs)
+                if timed:
+                    e0.record(self.stream)
+                if self.inner_events:
+                    em = self.mid_events[pos]
+                else:
+                    self.begin_graph.replay()
+                    em = torch.cuda.Event(enable_timing=True)
+                    if timed:
+                        em.record(self.stream)
+                self.graphs[pos].replay()
+                if timed:
+                    e1.record(self.stream)
+            if timed:
+                pending.append((pos, e0, em, e1))
             pos += 1
-        self.stream.synchronize()
+        collect()
         totals += self.counters_total()
-        ms = sum(a.elapsed_time(b) for a, b in evs)
-        return ms, len(evs), totals
+        return rows, totals
 
     def counters_total(self) -> np.ndarray:
         return self.buf.view("counters").cpu().numpy().astype(np.int64).sum(axis=0)
@@ -282,6 +326,8 @@ class GpuRun:
             e0.record(self.stream)
             with torch.cuda.stream(self.stream):
                 self.sel[pos].copy_(host_sel[pos], non_blocking=True)
+                if not self.inner_events:
+                    self.begin_graph.replay()
                 self.graphs[pos].replay()
                 host_out.copy_(self.out, non_blocking=True)
             e1.record(self.stream)
@@ -297,11 +343,19 @@ class GpuRun:
         self.buf.close()
 
 
-def measure_link(hs, torch, host_ptr: int, nbytes: int) -> tuple:
-    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    zc, cp = hs.hs_probe_link(host_ptr, dev, nbytes, 5)
+def measure_link(hs, torch, host_ptr: int, nbytes: int, chunk: int = 1 << 30) -> tuple:
+    """Best zero-copy and memcpy host-to-device GB/s over the host buffer, read in chunks of at most 1 GiB
+    (so every page of the buffer is read at least once)."""
+    dev = torch.empty(min(nbytes, chunk), dtype=torch.uint8, device="cuda")
+    best_zc = best_cp = 0.0
+    for off in range(0, nbytes, chunk):
+        n = min(chunk, nbytes - off) // 16 * 16
+        if n < 16:
+            break
+        zc, cp = hs.hs_probe_link(host_ptr + off, dev, n, 3 if off else 5)
+        best_zc, best_cp = max(best_zc, zc), max(best_cp, cp)
     del dev
-    return zc, cp
+    return best_zc, best_cp
 
 
 def cpu_baseline(w: wl.Workload, budget_s: float = 12.0) -> dict:
@@ -418,6 +472,9 @@ def run_gpu(args) -> int:
     w = wl.WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
     run = GpuRun(w, prefetch=args.prefetch)
+    # The GPU reads the whole host pool once (as a long-running server has long since done), so that first-touch
+    # address translation of host pages is not charged to the timed steps; it also measures the link.
+    link_zc, link_cp = measure_link(hs, torch, run.buf.host.ptr, run.buf.host.nbytes // 16 * 16)
     # warm-up, then a cold start for the timed region
     run.run_steps(W, timed=False)
     run.reset()
@@ -430,17 +487,16 @@ def run_gpu(args) -> int:
 
     barrier()
     with ClockSampler(local) as clk:
-        per_step, _ = run.run_steps(K)
+        per_step, tot = run.run_steps(K)
         barrier()
-    step_ms = [ms for _, ms in per_step]
+    step_ms = [r[1] for r in per_step]
+    kern_ms = sum(r[2] for r in per_step)  # the resolve launches of every step, measured inside the timed region
     total_ms = max_over_ranks(sum(step_ms), dist)
     sel_per_step = w.layers * w.requests
     value = aggregate_rate(world, K * sel_per_step, total_ms)
+    n_launch = K * w.layers
 
-    # kernel-level pass: events around each hs_resolve launch, same steps, same flushes
-    kern_ms, n_launch, tot = run.kernel_pass(K)
     hits, misses, evictions, miss_bytes = (int(x) for x in tot)
-    link_zc, link_cp = measure_link(hs, torch, run.buf.host.ptr, min(run.buf.host.nbytes, 1 << 30) // 16 * 16)
     link_peak = max(link_zc, link_cp)
     meta = n_launch * meta_bytes_per_launch(w, w.requests) + 4 * hits + 16 * misses
     hbm_bytes = meta + miss_bytes
@@ -454,10 +510,15 @@ def run_gpu(args) -> int:
         "peak": link_peak if bound == "host_link" else hbm_peak,
         "unit": "GB/s",
         "frac": max(t_link, t_hbm) / kern_s,
-        "traffic": None,
+        "traffic": captured_traffic(w, sum(w.layers for r in per_step if r[0] == 0),
+                                    sum(w.layers for r in per_step if r[0] != 0)),
+        "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed ncu capture "
+                          "(profiles/), null unless taken on these kernel sources",
         "kernel": "hs_resolve_kernel",
         "kernel_ms_per_launch": kern_ms / n_launch,
         "launches": n_launch,
+        "timing": ("CUDA events inside the timed region: from the end of hs_step_begin to the end of the step's "
+                   "resolves" + (" (layer-wise prefetch included)" if args.prefetch else "")),
         "algorithmic_bytes_per_launch": {"link": miss_bytes / n_launch, "hbm": hbm_bytes / n_launch},
         "peak_source": f"host link measured in this run (zero-copy {link_zc:.1f}, memcpy {link_cp:.1f} GB/s); "
                        f"HBM {hbm_peak:.1f} GB/s {hbm_src}",
@@ -480,12 +541,11 @@ def run_gpu(args) -> int:
         nrun.run_steps(W, timed=False)
         nrun.reset()
         nper, _ = nrun.run_steps(K)
-        nms = sum(ms for _, ms in nper)
-        nk_ms, nk_launch, _ = nrun.kernel_pass(K)
+        nms = max_over_ranks(sum(r[1] for r in nper), dist)
+        nk_ms = sum(r[2] for r in nper)
         n_hbm = meta + 2 * miss_bytes
-        nms = max_over_ranks(nms, dist)
         noio = {"value": aggregate_rate(world, K * sel_per_step, nms), "unit": UNIT, "ms_per_step": nms / K,
-                "kernel_ms_per_launch": nk_ms / nk_launch,
+                "kernel_ms_per_launch": nk_ms / n_launch,
                 "roofline": {"bound": "hbm", "achieved": n_hbm / (nk_ms / 1e3) / 1e9, "peak": hbm_peak,
                              "unit": "GB/s", "frac": (n_hbm / (hbm_peak * 1e9)) / (nk_ms / 1e3)}}
         nrun.buf.host = None
@@ -493,8 +553,8 @@ def run_gpu(args) -> int:
     host.close()
 
     clocks = clk.summary()
-    cold = [ms for p, ms in per_step if p == 0]
-    steady = [ms for p, ms in per_step if p != 0]
+    cold = [r[1] for r in per_step if r[0] == 0]
+    steady = [r[1] for r in per_step if r[0] != 0]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -508,6 +568,7 @@ def run_gpu(args) -> int:
         "miss_gbs": miss_bytes / (total_ms / 1e3) / 1e9 * world,
         "cold_step_ms": statistics.mean(cold) if cold else None,
         "steady_step_ms": statistics.mean(steady) if steady else None,
+        "steady_step_ms_p10_p50_p90": ([float(np.percentile(steady, q)) for q in (10, 50, 90)] if steady else None),
         "roofline": roofline,
         "noio": noio,
         "e2e": e2e,

@@ -12,7 +12,7 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SOURCES = [os.path.join(HERE, "csrc", "hs_resolve.cu")]
-HEADERS = [os.path.join(ROOT, "include", "hs.h")]
+HEADERS = [os.path.join(ROOT, "include", "hs.h"), os.path.join(HERE, "csrc", "hs_block.cuh")]
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libhs.so")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -3,28 +3,39 @@
 // Method: "HiSparse: Scaling Sparse-Attention Decoding with Hierarchical KV Cache Management" (Abstract): a
 // fused CUDA kernel resolves each layer's selections -- hit detection, LRU replacement and host-to-device
 // fetches -- inside the decode CUDA graph; only the missing rows that hit the top-k are fetched ("HiSparse"
-// knowledge card, Timeline). The policy details (stamps = decode step, oldest stamp first with ties to the
-// lowest slot, misses paired with victims in ascending token order, empties first) are stated in hs.h.
+// knowledge card, Timeline). The policy (stamps = decode step, oldest stamp first with ties to the lowest slot,
+// misses paired with victims in ascending token order, empties first) is stated in hs.h.
 //
 // One launch resolves one layer for `batch` request-layers. A request-layer is served by a thread-block
-// cluster of `C` CTAs (C = 1, 2, 4 or 8, chosen by the host from the batch so that enough SMs issue host-link
-// loads). Every CTA of the cluster computes the full resolution redundantly from the same inputs, which is
-// deterministic, so the CTAs agree without exchanging data; a cluster barrier separates the last read of the
-// shared metadata from the first write, and the writes (metadata, out_slots, row copies) are partitioned
-// between the CTAs. There is no spin-wait anywhere.
+// cluster of C CTAs (C = 1, 2, 4 or 8, chosen by the host so that enough SMs issue host-link loads while the
+// grid stays within one wave). Every CTA of the cluster computes the whole resolution redundantly from the same
+// inputs -- deterministic, so the CTAs agree without exchanging data; a cluster barrier separates the last
+// read of the shared metadata from the first write, and the writes and row copies are partitioned by CTA rank.
+// There is no spin-wait anywhere.
 //
-// Per CTA, in shared memory:
-//   1. load the selection row, the slot stamps and slot tokens; clear the hit bitmap;
-//   2. gather tok2slot for every selected token (random 4-byte reads); mark hit slots in the bitmap, which
-//      also exposes a token selected twice among the hits;
-//   3. stable LSD radix sort (8-bit digits, warp match + per-warp digit tables) of the miss positions by
-//      token; the first pass filters the misses out of the selection (compaction fused with the sort);
-//   4. stable LSD radix sort of the non-selected slots by stamp - min stamp; the first m are the victims in
-//      (stamp, slot) order, because the sort is stable over slot order;
-//   5. after the cluster barrier: hit stamps, miss assignment (unmap old token, map new, stamp), out_slots,
-//      counters; then the row copies as 16-byte vector loads from mapped host memory (ld.global.cv, so a
-//      host row is always fetched over the link, never served from a stale L2 line) straight into the hot
-//      buffer, COPY_UNROLL independent loads in flight per thread.
+// Per CTA (512 threads), in shared memory:
+//   1. load the selection row, slot stamps and slot tokens; clear the hit bitmap (and the token bitmap); each
+//      warp keeps the min and max stamp it saw;
+//   2. each warp gathers tok2slot for its run of selection entries (random 4-byte reads, several in flight per
+//      thread); a hit sets its slot's bit in the hit bitmap, a miss its token's bit in the token bitmap (a bit
+//      found set already is a repeated token);
+//   3. the misses in selection order, by ballots over the same runs (identical in every CTA of the cluster);
+//   4. two warp groups at once, each on its own named barrier:
+//      A (warps 0-7): at once the first wave of row loads from host memory into registers -- the link is busy
+//         while the resolution goes on -- then the rank of every miss among the misses by token: a running
+//         count over the token bitmap (contexts up to 2^18 units; longer ones radix-sort the misses by token);
+//      B (warps 8-15): the victims -- a stable LSD radix sort (8-bit digits, per-warp digit rows, ranks from
+//         ballots, so the order is exact and deterministic) of the slots not hit, keyed by stamp - min stamp
+//         (one pass while the stamps span fewer than 256 steps); the first m are the victims in (stamp, slot)
+//         order;
+//   5. group A, after the cluster barrier, per owned selection entry: a hit is stamped; a miss of rank j takes
+//      victim j (the old token is unmapped, the new one mapped, the slot stamped); out_slots in input order;
+//   6. rows: the row chunks are split between the cluster's CTAs in interleaved runs of blocks of
+//      32 x COPY_UNROLL chunks (a run covers a whole row when rows span several blocks);
+//      group B starts on this CTA's blocks past the first wave at once (no other CTA reads the hot buffer, so
+//      this needs no barrier), group A lands its first wave in the victims' slots after step 5 and joins;
+//      warps take blocks from a shared counter. Loads are 16-byte ld.global.cv (a host row always comes over
+//      the link, never from a stale L2 line), straight into the hot buffer.
 
 #include <cuda_runtime.h>
 
@@ -34,44 +45,47 @@
 #include <new>
 
 #include "../../include/hs.h"
+#include "hs_block.cuh"
 
 namespace {
 
-constexpr int NT = 512;                 // threads per CTA
-constexpr int NW = NT / 32;             // warps per CTA
-constexpr int RADIX = 256;              // digit values per radix pass
-constexpr int TBL_STRIDE = RADIX + 1;   // padded per-warp digit table row
-constexpr int COPY_UNROLL = 8;          // 16-byte loads in flight per thread in the copy loop
+using hs::bits_of;
+using hs::Group;
+using hs::NT;
+using hs::NW;
+using hs::RED_INTS;
+using hs::TBL_STRIDE;
+
+constexpr int COPY_UNROLL = 8;  // 16-byte loads in flight per thread in the copy loops
 constexpr int MAX_CLUSTER = 8;
+constexpr int GA_WARPS = NW / 2;                 // group A: miss ranks and the first wave of row loads
+constexpr int GA_THREADS = GA_WARPS * 32;
+constexpr int BITMAP_MAX_CTX = 1 << 18;          // longer contexts rank misses with the radix sort
+constexpr int MISC_BAD = 0, MISC_NCAND = 1, MISC_CBUF = 2, MISC_NEXT = 3, MISC_INTS = 4;
 
 struct ResolveArgs {
-  const int32_t* topk;      // [batch][k]
-  int32_t* out_slots;       // [batch][k] or nullptr (prefetch)
-  int32_t* tok2slot;        // layer base, [max_batch][ctx]
-  int32_t* slot_tok;        // layer base, [max_batch][slots]
-  int32_t* slot_stamp;      // layer base, [max_batch][slots]
+  const int32_t* topk;           // [batch][k]
+  int32_t* out_slots;            // [batch][k] or nullptr (prefetch)
+  int32_t* tok2slot;             // layer base, [max_batch][ctx]
+  int32_t* slot_tok;             // layer base, [max_batch][slots]
+  int32_t* slot_stamp;           // layer base, [max_batch][slots]
   unsigned long long* counters;  // layer's 4 counters
   const int32_t* step;
   int32_t* err;
-  const uint8_t* src;       // row source of this layer, request 0
+  const uint8_t* src;            // row source of this layer, request 0
   int64_t src_req_stride;
-  uint8_t* hot;             // layer base, [max_batch][slots][row_bytes]
+  uint8_t* hot;                  // layer base, [max_batch][slots][row_bytes]
   int32_t k, ctx, slots, row_bytes;
-  int32_t cluster;          // CTAs per request-layer
+  int32_t cluster;               // CTAs per request-layer
 };
 
-// Contexts up to this many selection units rank their misses with a shared-memory bitmap (one bit per unit plus
-// a 16-bit running count per 32 units); longer contexts use the radix sort.
-constexpr int BITMAP_MAX_CTX = 1 << 18;
+__host__ __device__ inline bool use_bitmap(int ctx) { return ctx <= BITMAP_MAX_CTX; }
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 // Shared-memory carve-up, identical on host and device.
 struct SmemLayout {
-  size_t sel, slot, stamp, stok, hit, mpos, rank, cidx, mscr, tbl, red, total;
+  size_t sel, slot, stamp, stok, hit, mpos, cidx, mscr, mscr2, mscr3, tbl, red, wstat, misc, total;
 };
-
-__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
-
-__host__ __device__ inline bool use_bitmap(int ctx) { return ctx <= BITMAP_MAX_CTX; }
 
 __host__ __device__ inline SmemLayout smem_layout(int k, int slots, int ctx) {
   SmemLayout L;
@@ -82,265 +96,24 @@ __host__ __device__ inline SmemLayout smem_layout(int k, int slots, int ctx) {
   L.stok = o;  o = align16(o + sizeof(int32_t) * slots);
   L.hit = o;   o = align16(o + sizeof(uint32_t) * ((slots + 31) / 32));
   L.mpos = o;  o = align16(o + sizeof(uint16_t) * k);
-  L.rank = o;  o = align16(o + sizeof(uint16_t) * k);
   L.cidx = o;  o = align16(o + sizeof(uint16_t) * 2 * slots);
-  L.mscr = o;
   if (use_bitmap(ctx)) {
     const size_t words = ((size_t)ctx + 31) / 32;
-    o = align16(o + sizeof(uint32_t) * words);
-    o = align16(o + sizeof(uint16_t) * words);
+    L.mscr = o;  o = align16(o + sizeof(uint32_t) * words);   // token bitmap
+    L.mscr2 = o; o = align16(o + sizeof(uint16_t) * words);   // misses below each word
+    L.mscr3 = o;
   } else {
-    o = align16(o + sizeof(uint16_t) * 2 * k);
+    L.mscr = o;  o = align16(o + sizeof(uint16_t) * 2 * k);   // radix ping-pong
+    L.mscr2 = o; o = align16(o + sizeof(uint16_t) * k);       // rank of each miss position
+    L.mscr3 = o;
   }
   L.tbl = o;   o = align16(o + sizeof(int32_t) * NW * TBL_STRIDE);
-  L.red = o;   o = align16(o + sizeof(int32_t) * 4 * (NW + 1));
+  L.red = o;   o = align16(o + sizeof(int32_t) * 2 * RED_INTS);
+  L.wstat = o; o = align16(o + sizeof(int32_t) * 4 * NW);
+  L.misc = o;  o = align16(o + sizeof(int32_t) * MISC_INTS);
   L.total = o;
   return L;
 }
-
-// ------------------------------------------------------------------------------------------------------------
-// Block-wide helpers (NT threads).
-// ------------------------------------------------------------------------------------------------------------
-__device__ __forceinline__ int block_sum(int v, int* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = __reduce_add_sync(0xffffffffu, v);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  int s = 0;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) s += red[w];
-  __syncthreads();
-  return s;
-}
-
-__device__ __forceinline__ unsigned block_or(unsigned v, int* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = __reduce_or_sync(0xffffffffu, v);
-  if (lane == 0) red[warp] = (int)v;
-  __syncthreads();
-  unsigned s = 0;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) s |= (unsigned)red[w];
-  __syncthreads();
-  return s;
-}
-
-// min and max of non-negative ints in one pass (v < 0 means "no value").
-__device__ __forceinline__ void block_minmax(int lo, int hi, int* red, int* out_lo, int* out_hi) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)lo);  // unsigned: "no value" (INT_MAX) stays largest
-  hi = __reduce_max_sync(0xffffffffu, hi);
-  if (lane == 0) {
-    red[warp] = lo;
-    red[NW + 1 + warp] = hi;
-  }
-  __syncthreads();
-  int a = 0x7fffffff, b = -1;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    a = min(a, red[w]);
-    b = max(b, red[NW + 1 + w]);
-  }
-  __syncthreads();
-  *out_lo = a;
-  *out_hi = b;
-}
-
-// Exclusive prefix sum over the block; *total receives the sum of all values.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* red, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) red[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < NW ? red[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < NW) red[lane] = w;
-  }
-  __syncthreads();
-  const int before = warp ? red[warp - 1] : 0;
-  *total = red[NW - 1];
-  __syncthreads();
-  return before + x - v;
-}
-
-// One stable counting-sort pass on the 8-bit digit at `shift`. Items come in order from `in` (or are the
-// indices 0..n-1 when in == nullptr), items failing keep() are dropped, and the survivors are written to `out`
-// grouped by digit, keeping their input order within a digit. Each warp owns a contiguous segment of the
-// input and its own digit-count row, so ranks are exact and deterministic without atomics. Returns the number
-// of survivors (the same on every thread).
-template <class Key, class Keep>
-__device__ int radix_pass(const uint16_t* __restrict__ in, int n, uint16_t* __restrict__ out, int shift, Key key,
-                          Keep keep, int* __restrict__ tbl, int* __restrict__ red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int seg = (n + NW - 1) / NW;
-  const int beg = min(n, warp * seg);
-  const int end = min(n, beg + seg);
-  int* wt = tbl + warp * TBL_STRIDE;
-  for (int d = lane; d < RADIX; d += 32) wt[d] = 0;
-  __syncwarp();
-  for (int base = beg; base < end; base += 32) {
-    const int i = base + lane;
-    int item = 0;
-    unsigned dig = RADIX;
-    if (i < end) {
-      item = in ? (int)in[i] : i;
-      if (keep(item)) dig = ((unsigned)key(item) >> shift) & (RADIX - 1);
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, dig);
-    if (dig < RADIX && lane == __ffs(peers) - 1) wt[dig] += __popc(peers);
-    __syncwarp();
-  }
-  __syncthreads();
-  // exclusive scan of the counts in (digit, warp) order
-  constexpr int PER = RADIX * NW / NT;
-  int cnt[PER];
-  int sum = 0;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    const int idx = threadIdx.x * PER + e;
-    cnt[e] = tbl[(idx % NW) * TBL_STRIDE + idx / NW];
-    sum += cnt[e];
-  }
-  int total;
-  int run = block_exclusive_scan(sum, red, &total);
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    const int idx = threadIdx.x * PER + e;
-    tbl[(idx % NW) * TBL_STRIDE + idx / NW] = run;
-    run += cnt[e];
-  }
-  __syncthreads();
-  for (int base = beg; base < end; base += 32) {
-    const int i = base + lane;
-    int item = 0;
-    unsigned dig = RADIX;
-    if (i < end) {
-      item = in ? (int)in[i] : i;
-      if (keep(item)) dig = ((unsigned)key(item) >> shift) & (RADIX - 1);
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, dig);
-    if (dig < RADIX) out[wt[dig] + __popc(peers & ((1u << lane) - 1u))] = (uint16_t)item;
-    __syncwarp();
-    if (dig < RADIX && lane == __ffs(peers) - 1) wt[dig] += __popc(peers);
-    __syncwarp();
-  }
-  __syncthreads();
-  return total;
-}
-
-// Full stable sort: pass 0 filters from the identity sequence 0..n-1 into buf[0]; further passes ping-pong.
-// Returns a pointer to the buffer holding the result and its length in *count.
-template <class Key, class Keep>
-__device__ uint16_t* radix_sort(int n, int key_bits, uint16_t* buf0, uint16_t* buf1, Key key, Keep keep, int* tbl,
-                                int* red, int* count) {
-  int c = radix_pass(nullptr, n, buf0, 0, key, keep, tbl, red);
-  uint16_t* cur = buf0;
-  uint16_t* nxt = buf1;
-  for (int shift = 8; shift < key_bits; shift += 8) {
-    radix_pass(cur, c, nxt, shift, key, [](int) { return true; }, tbl, red);
-    uint16_t* t = cur;
-    cur = nxt;
-    nxt = t;
-  }
-  *count = c;
-  return cur;
-}
-
-// Order-preserving compaction of the indices i in [0, n) with pred(i) into out; returns the count (same on all
-// threads). Each warp owns a contiguous segment; a ballot gives the in-warp offsets.
-template <class Pred>
-__device__ int block_compact(int n, uint16_t* __restrict__ out, Pred pred, int* __restrict__ red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int seg = (n + NW - 1) / NW;
-  const int beg = min(n, warp * seg);
-  const int end = min(n, beg + seg);
-  int c = 0;
-  for (int i = beg + lane; i < end; i += 32) c += pred(i) ? 1 : 0;
-  c = __reduce_add_sync(0xffffffffu, c);
-  if (lane == 0) red[warp] = c;
-  __syncthreads();
-  int run = 0, total = 0;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    const int x = red[w];
-    run += w < warp ? x : 0;
-    total += x;
-  }
-  __syncthreads();
-  for (int base = beg; base < end; base += 32) {
-    const int i = base + lane;
-    const bool f = i < end && pred(i);
-    const unsigned bal = __ballot_sync(0xffffffffu, f);
-    if (f) out[run + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)i;
-    run += __popc(bal);
-  }
-  __syncthreads();
-  return total;
-}
-
-// Rank of every miss among the misses by token, with a bitmap over the context: rank(t) = number of set bits
-// below t = running count of the word holding t + popcount of its lower bits. Also flags a token set twice.
-// mpos: miss positions (m of them); sel: selection row; rank_of_pos[pos] receives the rank.
-__device__ unsigned bitmap_ranks(int m, int ctx, const uint16_t* __restrict__ mpos, const int32_t* __restrict__ sel,
-                                 uint16_t* __restrict__ rank_of_pos, uint32_t* __restrict__ bits,
-                                 uint16_t* __restrict__ prefix, int* __restrict__ red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwords = (ctx + 31) >> 5;
-  unsigned bad = 0;
-  for (int w = threadIdx.x; w < nwords; w += NT) bits[w] = 0u;
-  __syncthreads();
-  for (int q = threadIdx.x; q < m; q += NT) {
-    const int t = sel[mpos[q]];
-    const uint32_t bit = 1u << (t & 31);
-    if (atomicOr(&bits[t >> 5], bit) & bit) bad |= HS_DEVERR_DUP;
-  }
-  __syncthreads();
-  const int seg = (nwords + NW - 1) / NW;
-  const int beg = min(nwords, warp * seg);
-  const int end = min(nwords, beg + seg);
-  int c = 0;
-  for (int w = beg + lane; w < end; w += 32) c += __popc(bits[w]);
-  c = __reduce_add_sync(0xffffffffu, c);
-  if (lane == 0) red[warp] = c;
-  __syncthreads();
-  int run = 0;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) run += w < warp ? red[w] : 0;
-  __syncthreads();
-  for (int base = beg; base < end; base += 32) {
-    const int w = base + lane;
-    const int p = w < end ? __popc(bits[w]) : 0;
-    int incl = p;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (w < end) prefix[w] = (uint16_t)(run + incl - p);
-    run += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  __syncthreads();
-  for (int q = threadIdx.x; q < m; q += NT) {
-    const int pos = mpos[q];
-    const int t = sel[pos];
-    const int w = t >> 5;
-    rank_of_pos[pos] = (uint16_t)(prefix[w] + __popc(bits[w] & ((1u << (t & 31)) - 1u)));
-  }
-  __syncthreads();
-  return bad;
-}
-
-__device__ __forceinline__ int bits_of(unsigned x) { return x ? 32 - __clz(x) : 0; }
 
 __device__ __forceinline__ uint4 load_row_chunk_host(const uint8_t* p) {
   uint4 r;
@@ -354,13 +127,35 @@ __device__ __forceinline__ uint4 load_row_chunk_device(const uint8_t* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
 }
 
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
-
 template <bool FROM_HOST>
 __device__ __forceinline__ uint4 load_row_chunk(const uint8_t* p) {
   return FROM_HOST ? load_row_chunk_host(p) : load_row_chunk_device(p);
 }
+
+// Every warp executes these as a whole (the .aligned forms).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Walk a chunk sequence c, c + S, c + 2S, ... as (row, chunk-in-row) pairs without a division per step.
+struct ChunkWalk {
+  int q, w, sq, sw, cpr;
+  __device__ __forceinline__ ChunkWalk(int c, int S, int cpr_) : cpr(cpr_) {
+    q = c / cpr;
+    w = c - q * cpr;
+    sq = S / cpr;
+    sw = S - sq * cpr;
+  }
+  __device__ __forceinline__ void next() {
+    q += sq;
+    w += sw;
+    if (w >= cpr) {
+      w -= cpr;
+      ++q;
+    }
+  }
+};
 
 template <bool FROM_HOST, bool BITMAP>
 __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) {
@@ -372,11 +167,20 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   int32_t* s_stok = reinterpret_cast<int32_t*>(smem + L.stok);
   uint32_t* s_hit = reinterpret_cast<uint32_t*>(smem + L.hit);
   uint16_t* s_mpos = reinterpret_cast<uint16_t*>(smem + L.mpos);
-  uint16_t* s_rank = reinterpret_cast<uint16_t*>(smem + L.rank);
   uint16_t* s_cidx = reinterpret_cast<uint16_t*>(smem + L.cidx);
-  uint8_t* s_mscr = smem + L.mscr;
   int* s_tbl = reinterpret_cast<int*>(smem + L.tbl);
   int* s_red = reinterpret_cast<int*>(smem + L.red);
+  int* s_wlo = reinterpret_cast<int*>(smem + L.wstat);
+  int* s_whi = s_wlo + NW;
+  int* s_wval = s_whi + NW;
+  int* s_wmiss = s_wval + NW;
+  int* s_misc = reinterpret_cast<int*>(smem + L.misc);
+  // bitmap ranking
+  uint32_t* s_bits = reinterpret_cast<uint32_t*>(smem + L.mscr);
+  uint16_t* s_below = reinterpret_cast<uint16_t*>(smem + L.mscr2);
+  // radix ranking
+  uint16_t* s_mbuf = reinterpret_cast<uint16_t*>(smem + L.mscr);
+  uint16_t* s_rank = reinterpret_cast<uint16_t*>(smem + L.mscr2);
 
   // Programmatic dependent launch: wait until the preceding kernel in the stream has completed and its writes
   // are visible, then let the next kernel start its launch while this one runs.
@@ -386,7 +190,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   const int C = a.cluster;
   const int rank = blockIdx.x % C;
   const int b = blockIdx.x / C;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = a.k, H = a.slots, ctx = a.ctx, R = a.row_bytes;
   const int32_t step = __ldcg(a.step);
   int32_t* t2s = a.tok2slot + (size_t)b * ctx;
@@ -396,170 +200,305 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   int32_t* out = a.out_slots ? a.out_slots + (size_t)b * k : nullptr;
   const uint8_t* src = a.src + (size_t)b * (size_t)a.src_req_stride;
   uint8_t* hot = a.hot + (size_t)b * (size_t)H * (size_t)R;
+  const int hwords = (H + 31) >> 5;
+  const int cwords = (ctx + 31) >> 5;
+  const int cpr = R >> 4;
+  // Selection entries are owned by the CTAs of the cluster in runs of 32 (entry i belongs to CTA (i / 32) % C),
+  // which write their metadata and out_slots. Row chunks go in blocks of BLK: block g belongs to CTA g % C.
+  constexpr int BLK = 32 * COPY_UNROLL;
+  auto owned = [&](int i) { return ((i >> 5) % C) == rank; };
+  // Each warp handles a contiguous run of selection entries in steps 2 and 3.
+  const int wseg = ((k + NW * 32 - 1) / (NW * 32)) * 32;
+  const int wbeg = min(k, warp * wseg);
+  const int wend = min(k, wbeg + wseg);
 
-  // 1. selection row, slot metadata, empty hit bitmap
+  // 1. selection row, slot metadata, empty bitmaps, per-warp stamp range
   unsigned bad = 0;
-  for (int i = tid; i < k; i += NT) {
-    const int32_t t = __ldcg(sel + i);
-    s_sel[i] = t;
-    if (t >= ctx) bad |= HS_DEVERR_RANGE;
+  if (tid < MISC_INTS) s_misc[tid] = 0;
+  for (int i0 = tid; i0 < k; i0 += 4 * NT) {
+    int32_t t[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) t[u] = i0 + u * NT < k ? __ldcg(sel + i0 + u * NT) : 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u * NT < k) {
+        s_sel[i0 + u * NT] = t[u];
+        if (t[u] >= ctx) bad |= HS_DEVERR_RANGE;
+      }
   }
-  for (int v = tid; v < H; v += NT) {
-    s_stamp[v] = __ldcg(stp + v);
-    s_stok[v] = __ldcg(s2t + v);
+  int lo = 0x7fffffff, hi = -1;
+  for (int v0 = tid; v0 < H; v0 += 4 * NT) {
+    int32_t st[4], tk[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = v0 + u * NT;
+      st[u] = v < H ? __ldcg(stp + v) : 0;
+      tk[u] = v < H ? __ldcg(s2t + v) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = v0 + u * NT;
+      if (v < H) {
+        s_stamp[v] = st[u];
+        s_stok[v] = tk[u];
+        lo = min(lo, st[u]);
+        hi = max(hi, st[u]);
+      }
+    }
   }
-  for (int w = tid; w < (H + 31) / 32; w += NT) s_hit[w] = 0u;
+  for (int w = tid; w < hwords; w += NT) s_hit[w] = 0u;
+  if (BITMAP)
+    for (int w = tid; w < cwords; w += NT) s_bits[w] = 0u;
+  lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) {
+    s_wlo[warp] = lo;
+    s_whi[warp] = hi;
+  }
   __syncthreads();
 
-  // 2. hit test
-  for (int i = tid; i < k; i += NT) {
-    const int32_t t = s_sel[i];
-    int32_t s = (t >= 0 && t < ctx) ? __ldcg(t2s + t) : -1;
-    if (s >= H) {
-      bad |= HS_DEVERR_STATE;
-      s = -1;
+  // 2. hit test over this warp's run of entries: hits mark their slot, misses their token
+  int nvalid = 0, nmiss = 0;
+  for (int i0 = wbeg; i0 < wend; i0 += 4 * 32) {
+    int32_t t[4], s[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * 32 + lane;
+      t[u] = i < wend ? s_sel[i] : -1;
+      s[u] = (t[u] >= 0 && t[u] < ctx) ? __ldcg(t2s + t[u]) : -1;
     }
-    s_slot[i] = s;
-    if (s >= 0) {
-      const uint32_t bit = 1u << (s & 31);
-      if (atomicOr(&s_hit[s >> 5], bit) & bit) bad |= HS_DEVERR_DUP;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * 32 + lane;
+      if (i >= wend) continue;
+      int32_t sl = s[u];
+      if (sl >= H) {
+        bad |= HS_DEVERR_STATE;
+        sl = -1;
+      }
+      s_slot[i] = sl;
+      if (sl >= 0) {
+        const uint32_t bit = 1u << (sl & 31);
+        if (atomicOr(&s_hit[sl >> 5], bit) & bit) bad |= HS_DEVERR_DUP;
+      } else if (t[u] >= 0 && t[u] < ctx) {
+        if (BITMAP) {
+          const uint32_t bit = 1u << (t[u] & 31);
+          if (atomicOr(&s_bits[t[u] >> 5], bit) & bit) bad |= HS_DEVERR_DUP;
+        }
+        ++nmiss;
+      }
+      nvalid += t[u] >= 0 ? 1 : 0;
     }
+  }
+  nvalid = __reduce_add_sync(0xffffffffu, nvalid);
+  nmiss = __reduce_add_sync(0xffffffffu, nmiss);
+  if (lane == 0) {
+    s_wval[warp] = nvalid;
+    s_wmiss[warp] = nmiss;
   }
   __syncthreads();
   // Every read of the cluster-shared metadata by this CTA has completed.
   if (C > 1) cluster_arrive();
 
-  // 3. misses in selection order
-  auto is_miss = [&](int i) { return s_slot[i] < 0 && s_sel[i] >= 0 && s_sel[i] < ctx; };
-  const int m = block_compact(k, s_mpos, is_miss, s_red);
+  // 3. the misses in selection order (the same list in every CTA of the cluster)
+  int m = 0, run = 0;
+  for (int w = 0; w < NW; ++w) {
+    const int x = s_wmiss[w];
+    run += w < warp ? x : 0;
+    m += x;
+  }
+  for (int base = wbeg; base < wend; base += 32) {
+    const int i = base + lane;
+    const bool f = i < wend && s_slot[i] < 0 && s_sel[i] >= 0 && s_sel[i] < ctx;
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    if (f) s_mpos[run + __popc(bal & hs::lanemask_lt())] = (uint16_t)i;
+    run += __popc(bal);
+  }
+  __syncthreads();
+  const int nchunk = m * cpr;  // 16-byte chunks of the rows; chunk c = chunk c % cpr of miss c / cpr
+  const int nblk = (nchunk + BLK - 1) / BLK;
+  // Blocks go to the CTAs in runs of RUN consecutive blocks (whole rows when rows span several blocks): run s
+  // belongs to CTA s % C. Local block n of this CTA is global block (rank + C * (n / RUN)) * RUN + n % RUN.
+  const int RUN = max(1, cpr / BLK);
+  const int nrun = (nblk + RUN - 1) / RUN;
+  const int my_runs = nrun > rank ? (nrun - rank + C - 1) / C : 0;
+  const int my_blocks =
+      my_runs ? (my_runs - 1) * RUN + min(RUN, nblk - (rank + C * (my_runs - 1)) * RUN) : 0;
+  auto global_block = [&](int n) { return (rank + C * (n / RUN)) * RUN + n % RUN; };
 
-  // 4. start this CTA's first wave of row loads now, so the host link is busy while the ranks and victims are
-  //    being worked out; chunk c is 16-byte chunk (c % cpr) of the (c / cpr)-th miss in selection order
-  const int cpr = R >> 4;
-  const long long nchunk = (long long)m * cpr;
-  const long long stride = (long long)C * NT;
-  const long long c_first = (long long)rank * NT + tid;
+  // 4. two warp groups at once
   uint4 pre[COPY_UNROLL];
+  if (warp < GA_WARPS) {
+    // A: the first wave of row loads (block number `warp` of this CTA), then the rank of every miss by token
+    const Group g{0, GA_WARPS, 1};
+    int* red = s_red;
+    if (warp < my_blocks) {
+      ChunkWalk cw(global_block(warp) * BLK + lane, 32, cpr);
 #pragma unroll
-  for (int u = 0; u < COPY_UNROLL; ++u) {
-    const long long c = c_first + u * stride;
-    if (c < nchunk) {
-      const int q = (int)(c / cpr);
-      const int w = (int)(c - (long long)q * cpr);
-      pre[u] = load_row_chunk<FROM_HOST>(src + (size_t)s_sel[s_mpos[q]] * (size_t)R + ((size_t)w << 4));
+      for (int u = 0; u < COPY_UNROLL; ++u) {
+        if (cw.q < m)
+          pre[u] = load_row_chunk<FROM_HOST>(src + (size_t)s_sel[s_mpos[cw.q]] * R + ((size_t)cw.w << 4));
+        cw.next();
+      }
     }
-  }
-
-  // 5. rank of each miss among the misses by token
-  if (BITMAP) {
-    uint32_t* bits = reinterpret_cast<uint32_t*>(s_mscr);
-    uint16_t* prefix = reinterpret_cast<uint16_t*>(s_mscr + align16(sizeof(uint32_t) * (size_t)((ctx + 31) >> 5)));
-    bad |= bitmap_ranks(m, ctx, s_mpos, s_sel, s_rank, bits, prefix, s_red);
+    if (BITMAP) {
+      const int seg = (cwords + GA_WARPS - 1) / GA_WARPS;
+      const int beg = min(cwords, warp * seg);
+      const int end = min(cwords, beg + seg);
+      int c = 0;
+      for (int w = beg + lane; w < end; w += 32) c += __popc(s_bits[w]);
+      c = __reduce_add_sync(0xffffffffu, c);
+      if (lane == 0) red[warp] = c;
+      g.sync();
+      int below = 0;
+      for (int w = 0; w < GA_WARPS; ++w) below += w < warp ? red[w] : 0;
+      for (int base = beg; base < end; base += 32) {
+        const int w = base + lane;
+        const int p = w < end ? __popc(s_bits[w]) : 0;
+        int incl = p;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (w < end) s_below[w] = (uint16_t)(below + incl - p);
+        below += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    } else {
+      int m2 = 0;
+      const uint16_t* order = hs::radix_sort(
+          g, m, bits_of((unsigned)(ctx - 1)), s_mbuf, s_mbuf + k, [&](int q) { return s_sel[s_mpos[q]]; },
+          [](int) { return true; }, s_tbl, red, &m2);
+      for (int j = g.tid(); j < m; j += GA_THREADS) {
+        const int pos = s_mpos[order[j]];
+        s_rank[pos] = (uint16_t)j;
+        if (j && s_sel[pos] == s_sel[s_mpos[order[j - 1]]]) bad |= HS_DEVERR_DUP;
+      }
+    }
+    if (tid == 0) s_misc[MISC_NEXT] = GA_WARPS;
   } else {
-    uint16_t* mbuf = reinterpret_cast<uint16_t*>(s_mscr);
-    int m2 = 0;
-    const uint16_t* midx = radix_sort(
-        m, bits_of((unsigned)(ctx - 1)), mbuf, mbuf + k, [&](int q) { return s_sel[s_mpos[q]]; },
-        [](int) { return true; }, s_tbl, s_red, &m2);
-    for (int j = tid; j < m; j += NT) {
-      const int pos = s_mpos[midx[j]];
-      s_rank[pos] = (uint16_t)j;
-      if (j && s_sel[pos] == s_sel[s_mpos[midx[j - 1]]]) bad |= HS_DEVERR_DUP;
+    // B: victims in (stamp, slot) order
+    const Group g{GA_WARPS, NW - GA_WARPS, 2};
+    int smin = 0x7fffffff, smax = -1;
+    for (int w = 0; w < NW; ++w) {
+      smin = min(smin, s_wlo[w]);
+      smax = max(smax, s_whi[w]);
     }
-    __syncthreads();
-  }
-
-  // 6. victims: non-selected slots by (stamp, slot)
-  int lo = 0x7fffffff, hi = -1;
-  for (int v = tid; v < H; v += NT) {
-    if (!(s_hit[v >> 5] & (1u << (v & 31)))) {
-      lo = min(lo, s_stamp[v]);
-      hi = max(hi, s_stamp[v]);
+    const int stamp_bits = smax >= smin ? bits_of((unsigned)(smax - smin)) : 0;
+    int ncand = 0;
+    const uint16_t* cidx = hs::radix_sort(
+        g, H, stamp_bits, s_cidx, s_cidx + H, [&](int v) { return s_stamp[v] - smin; },
+        [&](int v) { return !(s_hit[v >> 5] & (1u << (v & 31))); }, s_tbl, s_red + RED_INTS, &ncand);
+    if (g.tid() == 0) {
+      s_misc[MISC_NCAND] = ncand;
+      s_misc[MISC_CBUF] = cidx == s_cidx ? 0 : 1;
     }
   }
-  int smin, smax;
-  block_minmax(lo, hi, s_red, &smin, &smax);
-  int ncand = 0;
-  const int stamp_bits = smax >= smin ? bits_of((unsigned)(smax - smin)) : 0;
-  const uint16_t* cidx = radix_sort(
-      H, stamp_bits, s_cidx, s_cidx + H, [&](int v) { return s_stamp[v] - smin; },
-      [&](int v) { return !(s_hit[v >> 5] & (1u << (v & 31))); }, s_tbl, s_red, &ncand);
-  if (m > ncand) bad |= HS_DEVERR_STATE;
-  bad = block_or(bad, s_red);
-
-  if (C > 1) cluster_wait();  // no CTA of the cluster writes metadata before all have read it
+  if (bad) atomicOr(&s_misc[MISC_BAD], (int)bad);
+  __syncthreads();
+  const uint16_t* cidx = s_cidx + (s_misc[MISC_CBUF] ? H : 0);
+  bad = (unsigned)s_misc[MISC_BAD] | (m > s_misc[MISC_NCAND] ? HS_DEVERR_STATE : 0u);
 
   if (bad) {
-    for (int i = rank * NT + tid; i < k; i += C * NT)
-      if (out) out[i] = -1;
+    // a rejected row changes no metadata, so no cluster barrier is needed
+    if (out)
+      for (int i = tid; i < k; i += NT)
+        if (owned(i)) out[i] = -1;
     if (rank == 0 && tid == 0) atomicOr(a.err, (int)bad);
     return;
   }
 
-  // 7a. hits: stamp and emit
-  for (int i = rank * NT + tid; i < k; i += C * NT) {
-    const int32_t s = s_slot[i];
-    if (s >= 0) stp[s] = step;
-    if (out && (s >= 0 || s_sel[i] < 0)) out[i] = s;
-  }
-  // 7b. misses: the j-th smallest token takes the j-th victim
-  int nevict = 0;
-  for (int q = rank * NT + tid; q < m; q += C * NT) {
-    const int pos = s_mpos[q];
-    const int32_t t = s_sel[pos];
-    const int32_t v = cidx[s_rank[pos]];
-    const int32_t u = s_stok[v];
-    if (u >= 0) {
-      t2s[u] = -1;
-      ++nevict;
+  // victim of the miss at selection entry i holding token t
+  auto victim_of = [&](int i, int t) -> int {
+    int j;
+    if (BITMAP) {
+      const int w = t >> 5;
+      j = s_below[w] + __popc(s_bits[w] & ((1u << (t & 31)) - 1u));
+    } else {
+      j = s_rank[i];
     }
-    t2s[t] = v;
-    s2t[v] = t;
-    stp[v] = step;
-    if (out) out[pos] = v;
-  }
-  // 7c. the first wave of rows lands in its slots
+    return cidx[j];
+  };
+  auto store_chunk = [&](int q, int w, const uint4& val) {
+    const int i = s_mpos[q];
+    *reinterpret_cast<uint4*>(hot + (size_t)victim_of(i, s_sel[i]) * R + ((size_t)w << 4)) = val;
+  };
+
+  // this CTA's row blocks past the first wave, one per warp at a time from a shared counter
+  auto copy_rows = [&]() {
+    while (true) {
+      int n = 0;
+      if (lane == 0) n = atomicAdd(&s_misc[MISC_NEXT], 1);
+      n = __shfl_sync(0xffffffffu, n, 0);
+      if (n >= my_blocks) break;
+      uint4 v[COPY_UNROLL];
+      ChunkWalk cw(global_block(n) * BLK + lane, 32, cpr);
 #pragma unroll
-  for (int u = 0; u < COPY_UNROLL; ++u) {
-    const long long c = c_first + u * stride;
-    if (c < nchunk) {
-      const int q = (int)(c / cpr);
-      const int w = (int)(c - (long long)q * cpr);
-      const size_t v = cidx[s_rank[s_mpos[q]]];
-      *reinterpret_cast<uint4*>(hot + v * (size_t)R + ((size_t)w << 4)) = pre[u];
-    }
-  }
-  // 7d. the remaining rows, COPY_UNROLL loads in flight per thread
-  for (long long c0 = c_first + stride * COPY_UNROLL; c0 < nchunk; c0 += stride * COPY_UNROLL) {
-    uint4 v[COPY_UNROLL];
-    uint8_t* dst[COPY_UNROLL];
+      for (int u = 0; u < COPY_UNROLL; ++u) {
+        if (cw.q < m) v[u] = load_row_chunk<FROM_HOST>(src + (size_t)s_sel[s_mpos[cw.q]] * R + ((size_t)cw.w << 4));
+        cw.next();
+      }
+      ChunkWalk cs(global_block(n) * BLK + lane, 32, cpr);
 #pragma unroll
-    for (int u = 0; u < COPY_UNROLL; ++u) {
-      const long long c = c0 + u * stride;
-      dst[u] = nullptr;
-      if (c < nchunk) {
-        const int q = (int)(c / cpr);
-        const int w = (int)(c - (long long)q * cpr);
-        const int pos = s_mpos[q];
-        v[u] = load_row_chunk<FROM_HOST>(src + (size_t)s_sel[pos] * (size_t)R + ((size_t)w << 4));
-        dst[u] = hot + (size_t)cidx[s_rank[pos]] * (size_t)R + ((size_t)w << 4);
+      for (int u = 0; u < COPY_UNROLL; ++u) {
+        if (cs.q < m) store_chunk(cs.q, cs.w, v[u]);
+        cs.next();
       }
     }
-#pragma unroll
-    for (int u = 0; u < COPY_UNROLL; ++u)
-      if (dst[u]) *reinterpret_cast<uint4*>(dst[u]) = v[u];
-  }
-  nevict = block_sum(nevict, s_red);
-  int nvalid = 0;
-  for (int i = tid; i < k; i += NT) nvalid += s_sel[i] >= 0 ? 1 : 0;
-  nvalid = block_sum(nvalid, s_red);
-  if (tid == 0) {
-    if (nevict) atomicAdd(a.counters + 2, (unsigned long long)nevict);
-    if (rank == 0) {
-      atomicAdd(a.counters + 0, (unsigned long long)(nvalid - m));
-      atomicAdd(a.counters + 1, (unsigned long long)m);
-      atomicAdd(a.counters + 3, (unsigned long long)m * (unsigned long long)R);
+  };
+
+  int nevict = 0;
+  if (warp >= GA_WARPS) {
+    // B: rows past the first wave, at once (hot-buffer slots are read by no other CTA, so no barrier)
+    copy_rows();
+    if (C > 1) cluster_wait();
+  } else {
+    // A: 5. per owned selection entry, once every CTA of the cluster has read the metadata: hits are
+    //    stamped, a miss of rank j takes victim j
+    if (C > 1) cluster_wait();
+    for (int i = tid; i < k; i += GA_THREADS) {
+      if (!owned(i)) continue;
+      const int32_t t = s_sel[i];
+      const int32_t s = s_slot[i];
+      if (s >= 0) {
+        stp[s] = step;
+        if (out) out[i] = s;
+      } else if (t < 0) {
+        if (out) out[i] = -1;
+      } else {
+        const int32_t v = victim_of(i, t);
+        const int32_t u = s_stok[v];
+        if (u >= 0) {
+          t2s[u] = -1;
+          ++nevict;
+        }
+        t2s[t] = v;
+        s2t[v] = t;
+        stp[v] = step;
+        if (out) out[i] = v;
+      }
     }
+    // 6. the first wave lands in the victims' slots, then this group joins the copy
+    if (warp < my_blocks) {
+      ChunkWalk cw(global_block(warp) * BLK + lane, 32, cpr);
+#pragma unroll
+      for (int u = 0; u < COPY_UNROLL; ++u) {
+        if (cw.q < m) store_chunk(cw.q, cw.w, pre[u]);
+        cw.next();
+      }
+    }
+    copy_rows();
+  }
+
+  // counters
+  nevict = __reduce_add_sync(0xffffffffu, nevict);
+  if (lane == 0 && nevict) atomicAdd(a.counters + 2, (unsigned long long)nevict);
+  if (rank == 0 && tid == 0) {
+    int nv = 0;
+    for (int w = 0; w < NW; ++w) nv += s_wval[w];
+    atomicAdd(a.counters + 0, (unsigned long long)(nv - m));
+    atomicAdd(a.counters + 1, (unsigned long long)m);
+    atomicAdd(a.counters + 3, (unsigned long long)m * (unsigned long long)R);
   }
 }
 
@@ -609,7 +548,9 @@ struct hs_pool {
   int32_t* slot_tok;
   int32_t* slot_stamp;
   size_t smem;
-  int max_cluster;  // largest cluster size that fits on the device for this shared-memory size
+  int max_cluster;   // largest cluster size that fits on the device for this shared-memory size
+  int resident;      // resolve CTAs resident on the device at once (one wave)
+  int max_active[MAX_CLUSTER + 1];  // clusters of each size resident at once
 };
 
 namespace {
@@ -621,6 +562,9 @@ bool geometry_ok(const hs_pool_desc* d) {
   if (d->layers < 1 || d->max_batch < 1 || d->ctx < 1 || d->slots < 1 || d->topk_max < 1) return false;
   if (d->topk_max > d->slots || d->slots > 65535) return false;
   if (d->row_bytes <= 0 || (d->row_bytes & 15)) return false;
+  // the kernel numbers the 16-byte chunks of one request-layer's misses with int
+  if ((int64_t)d->topk_max * (d->row_bytes >> 4) > (int64_t)0x7fffffff - (int64_t)COPY_UNROLL * 2 * 8 * 512)
+    return false;
   if (d->host_layer_stride < 0 || (d->host_layer_stride & 15)) return false;
   if (d->host_req_stride < 0 || (d->host_req_stride & 15)) return false;
   return true;
@@ -686,10 +630,11 @@ int init_meta(hs_pool* p, cudaStream_t s) {
 }
 
 int pick_cluster(const hs_pool* p, int batch) {
-  // Enough CTAs to keep the host link (or HBM, in no-IO mode) busy; the link saturates with a few dozen SMs.
-  const int target = p->noio ? p->num_sms : 64;
+  // Enough CTAs to keep the host link (or HBM, in no-IO mode) busy -- the link saturates with a few dozen
+  // SMs -- without spilling the grid into a second wave.
+  const int target = p->noio ? p->resident : 64;
   int c = 1;
-  while (c < p->max_cluster && batch * c < target) c <<= 1;
+  while (c < p->max_cluster && batch * c < target && batch <= p->max_active[2 * c]) c <<= 1;
   return c;
 }
 
@@ -817,6 +762,16 @@ int hs_pool_create(const hs_pool_desc* desc, hs_stream_t stream, hs_pool** out) 
   p->slot_tok = reinterpret_cast<int32_t*>(base + lay.slot_tok);
   p->slot_stamp = reinterpret_cast<int32_t*>(base + lay.slot_stamp);
   p->smem = smem;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hs_resolve_kernel<true, true>, NT, smem) !=
+          cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  p->resident = per_sm * sms;
+  for (int c = 0; c <= MAX_CLUSTER; ++c) p->max_active[c] = 0;
+  p->max_active[1] = p->resident;
   // largest power-of-two cluster whose CTAs fit on the device at this shared-memory size
   p->max_cluster = 1;
   for (int c = 2; c <= MAX_CLUSTER; c <<= 1) {
@@ -839,6 +794,7 @@ int hs_pool_create(const hs_pool_desc* desc, hs_stream_t stream, hs_pool** out) 
     }
     if (n < 1) break;
     p->max_cluster = c;
+    p->max_active[c] = n;
   }
   const int rc = init_meta(p, reinterpret_cast<cudaStream_t>(stream));
   if (rc != HS_OK) {
