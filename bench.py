@@ -161,7 +161,7 @@ class GpuRun:
     """One pool for a workload, its per-step graphs, and the measurement passes."""
 
     def __init__(self, w: wl.Workload, noio: bool = False, prefetch: bool = False, host: object = None,
-                 host_layers: int | None = None):
+                 host_layers: int | None = None, layer_work_mb: float = 0.0, work_only: bool = False):
         import torch
 
         import hierarchical_sparse_attention_hs_gb300 as hs
@@ -183,6 +183,17 @@ class GpuRun:
         self.stream = torch.cuda.Stream()
         self.side = torch.cuda.Stream() if prefetch else None
         self.flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        # Stand-in for the rest of a decoder layer, run after each layer's resolve on the main stream: the
+        # sparse-attention read of the selected rows (hs_gather) plus a copy of layer_work_mb MB (the layer's
+        # other memory traffic). work_only replays the same per-layer work without any resolve.
+        self.layer_work = layer_work_mb > 0 or work_only
+        self.work_only = work_only
+        if self.layer_work:
+            self.gather_buf = torch.empty(w.requests * w.topk * w.row_bytes, dtype=torch.uint8, device="cuda")
+            nb = max(16, int(layer_work_mb * (1 << 20)) // 16 * 16)
+            self.work_src = torch.ones(nb, dtype=torch.uint8, device="cuda")
+            self.work_dst = torch.empty(nb, dtype=torch.uint8, device="cuda")
+            self.out.fill_(-1)
         torch.cuda.synchronize()
         self.graphs = [self._capture(s) for s in range(w.steps)]
         torch.cuda.synchronize()
@@ -192,35 +203,48 @@ class GpuRun:
 
     def enqueue(self, s):
         """Enqueue decode step s on self.stream: hs_step_begin, then the step's resolves."""
+        if self.work_only:
+            for l in range(self.w.layers):
+                self.enqueue_layer_work(l)
+            return
         self.hs.hs_step_begin(self.pool, self.stream)
         self.enqueue_resolves(s)
 
+    def enqueue_layer_work(self, l):
+        if not self.layer_work:
+            return
+        w = self.w
+        self.hs.hs_gather(self.pool, l, w.requests, self.out[l], w.topk, self.gather_buf, self.stream)
+        with self.torch.cuda.stream(self.stream):
+            self.work_dst.copy_(self.work_src)
+
     def enqueue_resolves(self, s):
-        """Enqueue the resolves of decode step s (all layers, all requests) on self.stream."""
+        """Enqueue the resolves of decode step s (all layers, all requests) on self.stream, each followed by the
+        layer's work stand-in when there is one."""
         torch, hs, w = self.torch, self.hs, self.w
         st = self.stream
         src = self.sel[s]
         if not self.prefetch:
             for l in range(w.layers):
                 hs.hs_resolve(self.pool, l, w.requests, src[self._lsel(l)], w.topk, self.out[l], st)
+                self.enqueue_layer_work(l)
             return
-        # exact layer-wise prefetch: layer l+1 resolves on the side stream while layer l resolves here
+        # exact layer-wise prefetch: once layer l starts on the main stream, layer l+1 is resolved on the side
+        # stream; layer l+1's own resolve waits for it and then only re-stamps and emits its slots
         side = self.side
-        ev0 = torch.cuda.Event()
-        ev0.record(st)
-        side.wait_event(ev0)
         done = [None] * w.layers
-        for l in range(1, w.layers):
-            hs.hs_prefetch(self.pool, l, w.requests, src[self._lsel(l)], w.topk, side)
-            done[l] = torch.cuda.Event()
-            done[l].record(side)
         for l in range(w.layers):
             if done[l] is not None:
                 st.wait_event(done[l])
+            if l + 1 < w.layers:
+                started = torch.cuda.Event()
+                started.record(st)
+                side.wait_event(started)
+                hs.hs_prefetch(self.pool, l + 1, w.requests, src[self._lsel(l + 1)], w.topk, side)
+                done[l + 1] = torch.cuda.Event()
+                done[l + 1].record(side)
             hs.hs_resolve(self.pool, l, w.requests, src[self._lsel(l)], w.topk, self.out[l], st)
-        evj = torch.cuda.Event()
-        evj.record(side)
-        st.wait_event(evj)
+            self.enqueue_layer_work(l)
 
     def _capture(self, s):
         """One graph per decode step: hs_step_begin, then the step's resolves (programmatic dependent launch lets
@@ -231,7 +255,9 @@ class GpuRun:
         return g
 
     def launches_per_step(self) -> int:
-        return 1 + self.w.layers + (self.w.layers - 1 if self.prefetch else 0)
+        if self.work_only:
+            return self.w.layers
+        return 1 + self.w.layers * (2 if self.layer_work else 1) + (self.w.layers - 1 if self.prefetch else 0)
 
     def flush(self):
         with self.torch.cuda.stream(self.stream):
@@ -442,7 +468,7 @@ def run_gpu(args) -> int:
 
     w = wl.WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
-    run = GpuRun(w, prefetch=args.prefetch)
+    run = GpuRun(w, prefetch=args.prefetch, layer_work_mb=args.layer_work_mb, work_only=args.work_only)
     # The GPU reads the whole host pool once (as a long-running server has long since done), so that first-touch
     # address translation of host pages is not charged to the timed steps; it also measures the link.
     link_zc, link_cp = measure_link(hs, torch, run.buf.host.ptr, run.buf.host.nbytes // 16 * 16)
@@ -511,7 +537,8 @@ def run_gpu(args) -> int:
     # no-IO mode on the same workload: misses sourced from an HBM copy of the pool
     noio = None
     if not args.skip_noio:
-        nrun = GpuRun(w, noio=True, prefetch=args.prefetch, host=host, host_layers=run.host_layers)
+        nrun = GpuRun(w, noio=True, prefetch=args.prefetch, host=host, host_layers=run.host_layers,
+                      layer_work_mb=args.layer_work_mb, work_only=args.work_only)
         nrun.run_steps(W, timed=False)
         nrun.reset()
         nper, _ = nrun.run_steps(K)
@@ -537,7 +564,8 @@ def run_gpu(args) -> int:
                    "l2": "flushed between steps (256 MiB write)",
                    "host_pool": ("one pool per layer" if run.host_layers == w.layers else
                                  "layers share one host pool (host_layer_stride 0); every miss still crosses the link"),
-                   "graphs": "one CUDA graph per decode step", "prefetch": bool(args.prefetch)},
+                   "graphs": "one CUDA graph per decode step", "prefetch": bool(args.prefetch),
+                   "layer_work_mb": args.layer_work_mb, "work_only": bool(args.work_only)},
         "selected_entries_per_s": value * w.topk,
         "miss_gbs": miss_bytes / (total_ms / 1e3) / 1e9 * world,
         "cold_step_ms": statistics.mean(cold) if cold else None,
@@ -566,6 +594,10 @@ def main() -> int:
     ap.add_argument("--impl", choices=["hs", "reference"], default="hs")
     ap.add_argument("--workload", choices=list(wl.WORKLOADS), default="dsa")
     ap.add_argument("--prefetch", action="store_true", help="layer-wise prefetch on a second stream")
+    ap.add_argument("--layer-work-mb", type=float, default=0.0,
+                    help="per-layer work stand-in after each resolve: hs_gather + a copy of this many MB")
+    ap.add_argument("--work-only", action="store_true",
+                    help="replay only the per-layer work stand-in (no resolve): the reference for exposed time")
     ap.add_argument("--skip-noio", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)

@@ -20,7 +20,7 @@ __all__ = [
     "HsError", "hs_pool_desc", "hs_meta_layout", "load", "hs_meta_bytes", "hs_get_meta_layout", "hs_pool_create",
     "hs_pool_reset", "hs_step_begin", "hs_resolve", "hs_prefetch", "hs_get_error", "hs_get_counters",
     "hs_pool_destroy", "hs_host_alloc", "hs_host_free", "hs_error_string", "HS_DEVERR_RANGE", "HS_DEVERR_DUP",
-    "HS_DEVERR_STATE", "HostBuffer", "PoolBuffers", "hs_probe_link",
+    "HS_DEVERR_STATE", "HostBuffer", "PoolBuffers", "hs_probe_link", "hs_gather", "hs_gather_history",
 ]
 
 HS_OK = 0
@@ -76,6 +76,8 @@ def load():
             "hs_step_begin": (ctypes.c_int, [vp, vp]),
             "hs_resolve": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp]),
             "hs_prefetch": (ctypes.c_int, [vp, i32, i32, vp, i32, vp]),
+            "hs_gather": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp]),
+            "hs_gather_history": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp]),
             "hs_get_error": (ctypes.c_int, [vp, P(i32), i32]),
             "hs_get_counters": (ctypes.c_int, [vp, i32, P(ctypes.c_uint64)]),
             "hs_pool_destroy": (ctypes.c_int, [vp]),
@@ -158,6 +160,15 @@ def hs_resolve(pool: int, layer: int, batch: int, topk_idx, k: int, out_slots, s
 
 def hs_prefetch(pool: int, layer: int, batch: int, topk_idx, k: int, stream=None) -> None:
     _check(load().hs_prefetch(pool, layer, batch, _addr(topk_idx), k, _stream(stream)), "hs_prefetch")
+
+
+def hs_gather(pool: int, layer: int, batch: int, out_slots, k: int, dst, stream=None) -> None:
+    _check(load().hs_gather(pool, layer, batch, _addr(out_slots), k, _addr(dst), _stream(stream)), "hs_gather")
+
+
+def hs_gather_history(pool: int, layer: int, batch: int, topk_idx, k: int, dst, stream=None) -> None:
+    _check(load().hs_gather_history(pool, layer, batch, _addr(topk_idx), k, _addr(dst), _stream(stream)),
+           "hs_gather_history")
 
 
 def hs_get_error(pool: int, clear: bool = False) -> int:

@@ -39,6 +39,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
         cw.next();
       }
     }
-    if (BITMAP) {
+    if (BITMAP && m > 0) {
       const int seg = (cwords + GA_WARPS - 1) / GA_WARPS;
       const int beg = min(cwords, warp * seg);
       const int end = min(cwords, beg + seg);
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
         if (w < end) s_below[w] = (uint16_t)(below + incl - p);
         below += __shfl_sync(0xffffffffu, incl, 31);
       }
-    } else {
+    } else if (!BITMAP && m > 0) {
       int m2 = 0;
       const uint16_t* order = hs::radix_sort(
           g, m, bits_of((unsigned)(ctx - 1)), s_mbuf, s_mbuf + k, [&](int q) { return s_sel[s_mpos[q]]; },
@@ -386,9 +387,11 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     }
     const int stamp_bits = smax >= smin ? bits_of((unsigned)(smax - smin)) : 0;
     int ncand = 0;
-    const uint16_t* cidx = hs::radix_sort(
-        g, H, stamp_bits, s_cidx, s_cidx + H, [&](int v) { return s_stamp[v] - smin; },
-        [&](int v) { return !(s_hit[v >> 5] & (1u << (v & 31))); }, s_tbl, s_red + RED_INTS, &ncand);
+    const uint16_t* cidx = s_cidx;
+    if (m > 0)  // a call whose selection is all resident (a resolve after its prefetch) needs no victims
+      cidx = hs::radix_sort(
+          g, H, stamp_bits, s_cidx, s_cidx + H, [&](int v) { return s_stamp[v] - smin; },
+          [&](int v) { return !(s_hit[v >> 5] & (1u << (v & 31))); }, s_tbl, s_red + RED_INTS, &ncand);
     if (g.tid() == 0) {
       s_misc[MISC_NCAND] = ncand;
       s_misc[MISC_CBUF] = cidx == s_cidx ? 0 : 1;
@@ -499,6 +502,42 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     atomicAdd(a.counters + 0, (unsigned long long)(nv - m));
     atomicAdd(a.counters + 1, (unsigned long long)m);
     atomicAdd(a.counters + 3, (unsigned long long)m * (unsigned long long)R);
+  }
+}
+
+// Gather rows by index, the read a sparse-attention kernel makes: row i of request b goes to
+// dst[(b * k + i) * row_bytes]; an index < 0 or >= limit gives a zero row. Rows of request b start at
+// base + b * req_stride. 16-byte chunks, COPY_UNROLL loads in flight per thread.
+template <bool FROM_HOST>
+__global__ void hs_gather_kernel(const uint8_t* __restrict__ base, int64_t req_stride, int row_bytes,
+                                 const int32_t* __restrict__ idx, int k, int rows, int limit,
+                                 uint8_t* __restrict__ dst) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int cpr = row_bytes >> 4;
+  const long long n = (long long)rows * cpr;
+  const long long nth = (long long)gridDim.x * blockDim.x;
+  for (long long c0 = blockIdx.x * (long long)blockDim.x + threadIdx.x; c0 < n; c0 += nth * COPY_UNROLL) {
+    uint4 v[COPY_UNROLL];
+#pragma unroll
+    for (int u = 0; u < COPY_UNROLL; ++u) {
+      const long long c = c0 + u * nth;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < n) {
+        const int r = (int)(c / cpr);
+        const int w = (int)(c - (long long)r * cpr);
+        const int t = __ldcg(idx + r);
+        if (t >= 0 && t < limit) {
+          const uint8_t* p = base + (size_t)(r / k) * (size_t)req_stride + (size_t)t * row_bytes + ((size_t)w << 4);
+          v[u] = FROM_HOST ? load_row_chunk_host(p) : __ldcg(reinterpret_cast<const uint4*>(p));
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < COPY_UNROLL; ++u) {
+      const long long c = c0 + u * nth;
+      if (c < n) *reinterpret_cast<uint4*>(dst + ((size_t)c << 4)) = v[u];
+    }
   }
 }
 
@@ -834,6 +873,54 @@ int hs_resolve(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* topk_
 int hs_prefetch(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* topk_idx, int32_t k,
                 hs_stream_t stream) {
   return launch_resolve(pool, layer, batch, topk_idx, k, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static int launch_gather(hs_pool* p, int32_t layer, int32_t batch, const int32_t* idx, int32_t k, void* dst,
+                         hs_stream_t stream, bool history) {
+  if (!p || layer < 0 || layer >= p->d.layers || batch < 0 || batch > p->d.max_batch || k < 0 ||
+      k > p->d.topk_max)
+    return HS_ERR_INVALID_ARG;
+  if (batch == 0 || k == 0) return HS_OK;
+  if (!idx || !dst || (reinterpret_cast<uintptr_t>(dst) & 15)) return HS_ERR_INVALID_ARG;
+  const int rows = batch * k;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  const long long chunks = (long long)rows * (p->d.row_bytes >> 4);
+  const long long per_cta = (long long)NT * COPY_UNROLL;
+  cfg.gridDim = dim3((unsigned)std::min<long long>((chunks + per_cta - 1) / per_cta, 2LL * p->num_sms), 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  uint8_t* out = static_cast<uint8_t*>(dst);
+  cudaError_t e;
+  if (history) {
+    const uint8_t* base = p->src + (size_t)layer * (size_t)p->d.host_layer_stride;
+    const int64_t rs = p->d.host_req_stride ? p->d.host_req_stride : (int64_t)p->d.ctx * p->d.row_bytes;
+    e = p->noio ? cudaLaunchKernelEx(&cfg, hs_gather_kernel<false>, base, rs, p->d.row_bytes, idx, k, rows,
+                                     p->d.ctx, out)
+                : cudaLaunchKernelEx(&cfg, hs_gather_kernel<true>, base, rs, p->d.row_bytes, idx, k, rows,
+                                     p->d.ctx, out);
+  } else {
+    const size_t hrl = (size_t)p->d.slots * (size_t)p->d.row_bytes;
+    const uint8_t* base = static_cast<const uint8_t*>(p->d.hot_buf) + (size_t)layer * (size_t)p->d.max_batch * hrl;
+    e = cudaLaunchKernelEx(&cfg, hs_gather_kernel<false>, base, (int64_t)hrl, p->d.row_bytes, idx, k, rows,
+                           p->d.slots, out);
+  }
+  return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+int hs_gather(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* out_slots, int32_t k, void* dst,
+              hs_stream_t stream) {
+  return launch_gather(pool, layer, batch, out_slots, k, dst, stream, false);
+}
+
+int hs_gather_history(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* topk_idx, int32_t k, void* dst,
+                      hs_stream_t stream) {
+  return launch_gather(pool, layer, batch, topk_idx, k, dst, stream, true);
 }
 
 int hs_get_error(hs_pool* pool, int32_t* out, int32_t clear) {

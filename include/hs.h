@@ -151,6 +151,20 @@ int hs_resolve(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk_
 int hs_prefetch(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk_idx, int32_t k,
                 hs_stream_t stream);
 
+/*
+ * The read a sparse-attention kernel makes after a resolve: for every request b < batch and entry i < k, copy hot
+ * row out_slots[b][i] of `layer` to dst + (b*k + i)*row_bytes (a zero row for -1). dst: device memory of
+ * batch*k*row_bytes bytes, 16-byte aligned. Enqueued on `stream`. Together with hs_gather_history it shows that
+ * placement changes nothing the attention reads ("HiSparse" paper, Abstract: model outputs are unchanged).
+ */
+int hs_gather(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *out_slots, int32_t k, void *dst,
+              hs_stream_t stream);
+
+/* The same read from the full history: dst row (b, i) = host-pool row topk_idx[b][i] of `layer` (from the no-IO
+ * source when the pool has one; a zero row for an index < 0 or >= ctx). */
+int hs_gather_history(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk_idx, int32_t k, void *dst,
+                      hs_stream_t stream);
+
 /* Synchronise the device, then read the sticky device error word into *out (HS_DEVERR_* bits); clear it when
  * `clear` is non-zero. */
 int hs_get_error(hs_pool *pool, int32_t *out, int32_t clear);
