@@ -161,7 +161,8 @@ class GpuRun:
     """One pool for a workload, its per-step graphs, and the measurement passes."""
 
     def __init__(self, w: wl.Workload, noio: bool = False, prefetch: bool = False, host: object = None,
-                 host_layers: int | None = None, layer_work_mb: float = 0.0, work_only: bool = False):
+                 host_layers: int | None = None, layer_work_mb: float = 0.0, work_only: bool = False,
+                 full_offload: bool = False):
         import torch
 
         import hierarchical_sparse_attention_hs_gb300 as hs
@@ -188,6 +189,11 @@ class GpuRun:
         # other memory traffic). work_only replays the same per-layer work without any resolve.
         self.layer_work = layer_work_mb > 0 or work_only
         self.work_only = work_only
+        # Comparator without a GPU cache: every step fetches all selected rows of every layer from the host
+        # history (the traffic the resolution avoids), into a dense buffer.
+        self.full_offload = full_offload
+        if full_offload:
+            self.offload_buf = torch.empty(w.requests * w.topk * w.row_bytes, dtype=torch.uint8, device="cuda")
         if self.layer_work:
             self.gather_buf = torch.empty(w.requests * w.topk * w.row_bytes, dtype=torch.uint8, device="cuda")
             nb = max(16, int(layer_work_mb * (1 << 20)) // 16 * 16)
@@ -206,6 +212,12 @@ class GpuRun:
         if self.work_only:
             for l in range(self.w.layers):
                 self.enqueue_layer_work(l)
+            return
+        if self.full_offload:
+            w = self.w
+            for l in range(w.layers):
+                self.hs.hs_gather_history(self.pool, l, w.requests, self.sel[s][self._lsel(l)], w.topk,
+                                          self.offload_buf, self.stream)
             return
         self.hs.hs_step_begin(self.pool, self.stream)
         self.enqueue_resolves(s)
@@ -255,7 +267,7 @@ class GpuRun:
         return g
 
     def launches_per_step(self) -> int:
-        if self.work_only:
+        if self.work_only or self.full_offload:
             return self.w.layers
         return 1 + self.w.layers * (2 if self.layer_work else 1) + (self.w.layers - 1 if self.prefetch else 0)
 
@@ -468,7 +480,8 @@ def run_gpu(args) -> int:
 
     w = wl.WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
-    run = GpuRun(w, prefetch=args.prefetch, layer_work_mb=args.layer_work_mb, work_only=args.work_only)
+    run = GpuRun(w, prefetch=args.prefetch, layer_work_mb=args.layer_work_mb, work_only=args.work_only,
+                 full_offload=args.full_offload)
     # The GPU reads the whole host pool once (as a long-running server has long since done), so that first-touch
     # address translation of host pages is not charged to the timed steps; it also measures the link.
     link_zc, link_cp = measure_link(hs, torch, run.buf.host.ptr, run.buf.host.nbytes // 16 * 16)
@@ -496,6 +509,9 @@ def run_gpu(args) -> int:
     n_launch = K * w.layers
 
     hits, misses, evictions, miss_bytes = (int(x) for x in tot)
+    if args.full_offload:  # every selected row crossed the link
+        hits, misses = 0, K * w.layers * w.requests * w.topk
+        miss_bytes = misses * w.row_bytes
     link_peak = max(link_zc, link_cp)
     meta = n_launch * meta_bytes_per_launch(w, w.requests) + 4 * hits + 16 * misses
     hbm_bytes = meta + miss_bytes
@@ -538,7 +554,7 @@ def run_gpu(args) -> int:
     noio = None
     if not args.skip_noio:
         nrun = GpuRun(w, noio=True, prefetch=args.prefetch, host=host, host_layers=run.host_layers,
-                      layer_work_mb=args.layer_work_mb, work_only=args.work_only)
+                      layer_work_mb=args.layer_work_mb, work_only=args.work_only, full_offload=args.full_offload)
         nrun.run_steps(W, timed=False)
         nrun.reset()
         nper, _ = nrun.run_steps(K)
@@ -565,7 +581,8 @@ def run_gpu(args) -> int:
                    "host_pool": ("one pool per layer" if run.host_layers == w.layers else
                                  "layers share one host pool (host_layer_stride 0); every miss still crosses the link"),
                    "graphs": "one CUDA graph per decode step", "prefetch": bool(args.prefetch),
-                   "layer_work_mb": args.layer_work_mb, "work_only": bool(args.work_only)},
+                   "layer_work_mb": args.layer_work_mb, "work_only": bool(args.work_only),
+                   "full_offload": bool(args.full_offload)},
         "selected_entries_per_s": value * w.topk,
         "miss_gbs": miss_bytes / (total_ms / 1e3) / 1e9 * world,
         "cold_step_ms": statistics.mean(cold) if cold else None,
@@ -598,6 +615,8 @@ def main() -> int:
                     help="per-layer work stand-in after each resolve: hs_gather + a copy of this many MB")
     ap.add_argument("--work-only", action="store_true",
                     help="replay only the per-layer work stand-in (no resolve): the reference for exposed time")
+    ap.add_argument("--full-offload", action="store_true",
+                    help="comparator without a GPU cache: fetch every selected row from host memory every step")
     ap.add_argument("--skip-noio", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
