@@ -162,7 +162,7 @@ class GpuRun:
 
     def __init__(self, w: wl.Workload, noio: bool = False, prefetch: bool = False, host: object = None,
                  host_layers: int | None = None, layer_work_mb: float = 0.0, work_only: bool = False,
-                 full_offload: bool = False):
+                 full_offload: bool = False, shared_call: bool = False):
         import torch
 
         import hierarchical_sparse_attention_hs_gb300 as hs
@@ -192,6 +192,8 @@ class GpuRun:
         # Comparator without a GPU cache: every step fetches all selected rows of every layer from the host
         # history (the traffic the resolution avoids), into a dense buffer.
         self.full_offload = full_offload
+        # Layers that share one selection resolved by a single hs_resolve_shared call per step
+        self.shared_call = shared_call and w.shared_across_layers
         if full_offload:
             self.offload_buf = torch.empty(w.requests * w.topk * w.row_bytes, dtype=torch.uint8, device="cuda")
         if self.layer_work:
@@ -236,6 +238,11 @@ class GpuRun:
         torch, hs, w = self.torch, self.hs, self.w
         st = self.stream
         src = self.sel[s]
+        if self.shared_call:
+            hs.hs_resolve_shared(self.pool, 0, w.layers, w.requests, src[0], w.topk, self.out[0], st)
+            for l in range(w.layers):
+                self.enqueue_layer_work(l)
+            return
         if not self.prefetch:
             for l in range(w.layers):
                 hs.hs_resolve(self.pool, l, w.requests, src[self._lsel(l)], w.topk, self.out[l], st)
@@ -269,6 +276,8 @@ class GpuRun:
     def launches_per_step(self) -> int:
         if self.work_only or self.full_offload:
             return self.w.layers
+        if self.shared_call:
+            return 2 + (self.w.layers if self.layer_work else 0)
         return 1 + self.w.layers * (2 if self.layer_work else 1) + (self.w.layers - 1 if self.prefetch else 0)
 
     def flush(self):
@@ -481,7 +490,7 @@ def run_gpu(args) -> int:
     w = wl.WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
     run = GpuRun(w, prefetch=args.prefetch, layer_work_mb=args.layer_work_mb, work_only=args.work_only,
-                 full_offload=args.full_offload)
+                 full_offload=args.full_offload, shared_call=args.shared_call)
     # The GPU reads the whole host pool once (as a long-running server has long since done), so that first-touch
     # address translation of host pages is not charged to the timed steps; it also measures the link.
     link_zc, link_cp = measure_link(hs, torch, run.buf.host.ptr, run.buf.host.nbytes // 16 * 16)
@@ -506,7 +515,8 @@ def run_gpu(args) -> int:
     total_ms = max_over_ranks(sum(step_ms), dist)
     sel_per_step = w.layers * w.requests
     value = aggregate_rate(world, K * sel_per_step, total_ms)
-    n_launch = K * w.layers
+    n_launch = K * w.layers  # per-layer resolutions (one launch each, or one launch per step with --shared-call)
+    n_kernels = K if run.shared_call else n_launch
 
     hits, misses, evictions, miss_bytes = (int(x) for x in tot)
     if args.full_offload:  # every selected row crossed the link
@@ -530,12 +540,12 @@ def run_gpu(args) -> int:
         "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed ncu capture "
                           "(profiles/), null unless taken on these kernel sources",
         "kernel": "hs_resolve_kernel",
-        "kernel_ms_per_launch": kern_ms / n_launch,
-        "launches": n_launch,
+        "kernel_ms_per_launch": kern_ms / n_kernels,
+        "launches": n_kernels,
         "timing": ("CUDA events around each step's graph in the timed region: hs_step_begin plus the step's "
                    "resolves, an upper bound on the resolve launches" +
                    (" (layer-wise prefetch included)" if args.prefetch else "")),
-        "algorithmic_bytes_per_launch": {"link": miss_bytes / n_launch, "hbm": hbm_bytes / n_launch},
+        "algorithmic_bytes_per_launch": {"link": miss_bytes / n_kernels, "hbm": hbm_bytes / n_kernels},
         "peak_source": f"host link measured in this run (zero-copy {link_zc:.1f}, memcpy {link_cp:.1f} GB/s); "
                        f"HBM {hbm_peak:.1f} GB/s {hbm_src}",
     }
@@ -554,7 +564,8 @@ def run_gpu(args) -> int:
     noio = None
     if not args.skip_noio:
         nrun = GpuRun(w, noio=True, prefetch=args.prefetch, host=host, host_layers=run.host_layers,
-                      layer_work_mb=args.layer_work_mb, work_only=args.work_only, full_offload=args.full_offload)
+                      layer_work_mb=args.layer_work_mb, work_only=args.work_only, full_offload=args.full_offload,
+                      shared_call=args.shared_call)
         nrun.run_steps(W, timed=False)
         nrun.reset()
         nper, _ = nrun.run_steps(K)
@@ -562,7 +573,7 @@ def run_gpu(args) -> int:
         nk_ms = sum(r[1] for r in nper)
         n_hbm = meta + 2 * miss_bytes
         noio = {"value": aggregate_rate(world, K * sel_per_step, nms), "unit": UNIT, "ms_per_step": nms / K,
-                "kernel_ms_per_launch": nk_ms / n_launch,
+                "kernel_ms_per_launch": nk_ms / n_kernels,
                 "roofline": {"bound": "hbm", "achieved": n_hbm / (nk_ms / 1e3) / 1e9, "peak": hbm_peak,
                              "unit": "GB/s", "frac": (n_hbm / (hbm_peak * 1e9)) / (nk_ms / 1e3)}}
         nrun.buf.host = None
@@ -582,7 +593,7 @@ def run_gpu(args) -> int:
                                  "layers share one host pool (host_layer_stride 0); every miss still crosses the link"),
                    "graphs": "one CUDA graph per decode step", "prefetch": bool(args.prefetch),
                    "layer_work_mb": args.layer_work_mb, "work_only": bool(args.work_only),
-                   "full_offload": bool(args.full_offload)},
+                   "full_offload": bool(args.full_offload), "shared_call": bool(args.shared_call)},
         "selected_entries_per_s": value * w.topk,
         "miss_gbs": miss_bytes / (total_ms / 1e3) / 1e9 * world,
         "cold_step_ms": statistics.mean(cold) if cold else None,
@@ -615,6 +626,8 @@ def main() -> int:
                     help="per-layer work stand-in after each resolve: hs_gather + a copy of this many MB")
     ap.add_argument("--work-only", action="store_true",
                     help="replay only the per-layer work stand-in (no resolve): the reference for exposed time")
+    ap.add_argument("--shared-call", action="store_true",
+                    help="workloads whose layers share one selection: one hs_resolve_shared call per step")
     ap.add_argument("--full-offload", action="store_true",
                     help="comparator without a GPU cache: fetch every selected row from host memory every step")
     ap.add_argument("--skip-noio", action="store_true")

@@ -126,9 +126,14 @@ __device__ __forceinline__ unsigned digit_peers(unsigned dig, bool valid, int nb
 // by digit, in input order within a digit. Each warp owns a contiguous input segment and a digit-count row of
 // tbl (rows of the group's warps): counts by shared atomics (order-free), ranks inside a warp from ballots, so
 // the order is exact and deterministic. Returns the survivor count.
+//
+// With limit >= 0, only the first `limit` output positions are needed: items whose digit lies above the digit
+// holding position limit - 1 are not written, and a chunk of 32 items with none below it is skipped after one
+// ballot. (Only meaningful for the last pass of a sort.)
 template <class Key, class Keep>
 __device__ int radix_pass(const Group& g, const uint16_t* __restrict__ in, int n, uint16_t* __restrict__ out,
-                          int shift, int nbits, Key key, Keep keep, int* __restrict__ tbl, int* __restrict__ red) {
+                          int shift, int nbits, Key key, Keep keep, int* __restrict__ tbl, int* __restrict__ red,
+                          int limit = -1) {
   const int lane = threadIdx.x & 31, warp = g.warp();
   const int seg = (n + g.nw - 1) / g.nw;
   const int beg = min(n, warp * seg);
@@ -162,6 +167,24 @@ __device__ int radix_pass(const Group& g, const uint16_t* __restrict__ in, int n
     run += cnt[e];
   }
   g.sync();
+  // highest digit still needed: the one whose range of output positions holds position limit - 1
+  unsigned top = dmask;
+  if (limit >= 0) {
+    if (limit == 0) {
+      g.sync();
+      return total;
+    }
+    const int* first = tbl + g.w0 * TBL_STRIDE;  // first warp's row: exclusive start of each digit
+    int lo = 0, hi = (int)dmask;
+    while (lo < hi) {  // largest d with start(d) <= limit - 1
+      const int mid = (lo + hi + 1) >> 1;
+      if (first[mid] <= limit - 1)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    top = (unsigned)lo;
+  }
   for (int base = beg; base < end; base += 32) {
     const int i = base + lane;
     int item = 0;
@@ -172,6 +195,8 @@ __device__ int radix_pass(const Group& g, const uint16_t* __restrict__ in, int n
       valid = keep(item);
       if (valid) dig = ((unsigned)key(item) >> shift) & dmask;
     }
+    valid = valid && dig <= top;
+    if (limit >= 0 && !__ballot_sync(0xffffffffu, valid)) continue;
     const unsigned peers = digit_peers(dig, valid, nbits);
     if (valid) out[wt[dig] + __popc(peers & lanemask_lt())] = (uint16_t)item;
     __syncwarp();
@@ -183,11 +208,14 @@ __device__ int radix_pass(const Group& g, const uint16_t* __restrict__ in, int n
 }
 
 // Stable LSD sort on the low key_bits bits: pass 0 filters the identity sequence 0..n-1 into buf0, later passes
-// ping-pong. Returns the buffer holding the result; *count = its length.
+// ping-pong. Returns the buffer holding the result; *count = the number of items kept (with a limit, only the
+// first `limit` positions of the result are guaranteed).
 template <class Key, class Keep>
 __device__ uint16_t* radix_sort(const Group& g, int n, int key_bits, uint16_t* buf0, uint16_t* buf1, Key key,
-                                Keep keep, int* tbl, int* red, int* count) {
-  int c = radix_pass(g, nullptr, n, buf0, 0, min(8, max(key_bits, 0)), key, keep, tbl, red);
+                                Keep keep, int* tbl, int* red, int* count, int limit = -1) {
+  // a limit only applies to a single-pass sort (the pass that fixes the final order)
+  int c = radix_pass(g, nullptr, n, buf0, 0, min(8, max(key_bits, 0)), key, keep, tbl, red,
+                     key_bits <= 8 ? limit : -1);
   uint16_t* cur = buf0;
   uint16_t* nxt = buf1;
   for (int shift = 8; shift < key_bits; shift += 8) {

@@ -78,6 +78,13 @@ struct ResolveArgs {
   uint8_t* hot;                  // layer base, [max_batch][slots][row_bytes]
   int32_t k, ctx, slots, row_bytes;
   int32_t cluster;               // CTAs per request-layer
+  // Layers resolved by this launch: layer 0 of the args and the nlayers - 1 after it, whose caches hold the same
+  // metadata (they are always resolved together with one shared selection). Strides between layers.
+  int32_t nlayers;
+  int64_t meta_layer_ctx;        // int32 elements between layers in tok2slot
+  int64_t meta_layer_slots;      // int32 elements between layers in slot_tok / slot_stamp
+  int64_t src_layer_bytes;       // bytes between layers in the row source
+  int64_t hot_layer_bytes;       // bytes between layers in the hot buffer
 };
 
 __host__ __device__ inline bool use_bitmap(int ctx) { return ctx <= BITMAP_MAX_CTX; }
@@ -376,7 +383,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
         if (j && s_sel[pos] == s_sel[s_mpos[order[j - 1]]]) bad |= HS_DEVERR_DUP;
       }
     }
-    if (tid == 0) s_misc[MISC_NEXT] = GA_WARPS;
+    if (tid == 0) s_misc[MISC_NEXT] = min(GA_WARPS, my_blocks);  // the first wave took blocks [0, this)
   } else {
     // B: victims in (stamp, slot) order
     const Group g{GA_WARPS, NW - GA_WARPS, 2};
@@ -391,7 +398,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     if (m > 0)  // a call whose selection is all resident (a resolve after its prefetch) needs no victims
       cidx = hs::radix_sort(
           g, H, stamp_bits, s_cidx, s_cidx + H, [&](int v) { return s_stamp[v] - smin; },
-          [&](int v) { return !(s_hit[v >> 5] & (1u << (v & 31))); }, s_tbl, s_red + RED_INTS, &ncand);
+          [&](int v) { return !(s_hit[v >> 5] & (1u << (v & 31))); }, s_tbl, s_red + RED_INTS, &ncand, m);
     if (g.tid() == 0) {
       s_misc[MISC_NCAND] = ncand;
       s_misc[MISC_CBUF] = cidx == s_cidx ? 0 : 1;
@@ -422,29 +429,36 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     }
     return cidx[j];
   };
-  auto store_chunk = [&](int q, int w, const uint4& val) {
+  auto store_chunk_to = [&](uint8_t* dst_hot, int q, int w, const uint4& val) {
     const int i = s_mpos[q];
-    *reinterpret_cast<uint4*>(hot + (size_t)victim_of(i, s_sel[i]) * R + ((size_t)w << 4)) = val;
+    *reinterpret_cast<uint4*>(dst_hot + (size_t)victim_of(i, s_sel[i]) * R + ((size_t)w << 4)) = val;
   };
+  auto store_chunk = [&](int q, int w, const uint4& val) { store_chunk_to(hot, q, w, val); };
 
-  // this CTA's row blocks past the first wave, one per warp at a time from a shared counter
+  // this CTA's row blocks past the first wave, one per warp at a time from a shared counter; with several
+  // layers, local block n is block n % my_blocks of layer n / my_blocks
+  const int nl = a.nlayers;
   auto copy_rows = [&]() {
     while (true) {
       int n = 0;
       if (lane == 0) n = atomicAdd(&s_misc[MISC_NEXT], 1);
       n = __shfl_sync(0xffffffffu, n, 0);
-      if (n >= my_blocks) break;
+      if (n >= my_blocks * nl) break;
+      const int l = n / my_blocks;
+      const int nb = n - l * my_blocks;
+      const uint8_t* src_l = src + (size_t)l * (size_t)a.src_layer_bytes;
+      uint8_t* hot_l = hot + (size_t)l * (size_t)a.hot_layer_bytes;
       uint4 v[COPY_UNROLL];
-      ChunkWalk cw(global_block(n) * BLK + lane, 32, cpr);
+      ChunkWalk cw(global_block(nb) * BLK + lane, 32, cpr);
 #pragma unroll
       for (int u = 0; u < COPY_UNROLL; ++u) {
-        if (cw.q < m) v[u] = load_row_chunk<FROM_HOST>(src + (size_t)s_sel[s_mpos[cw.q]] * R + ((size_t)cw.w << 4));
+        if (cw.q < m) v[u] = load_row_chunk<FROM_HOST>(src_l + (size_t)s_sel[s_mpos[cw.q]] * R + ((size_t)cw.w << 4));
         cw.next();
       }
-      ChunkWalk cs(global_block(n) * BLK + lane, 32, cpr);
+      ChunkWalk cs(global_block(nb) * BLK + lane, 32, cpr);
 #pragma unroll
       for (int u = 0; u < COPY_UNROLL; ++u) {
-        if (cs.q < m) store_chunk(cs.q, cs.w, v[u]);
+        if (cs.q < m) store_chunk_to(hot_l, cs.q, cs.w, v[u]);
         cs.next();
       }
     }
@@ -464,20 +478,22 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
       const int32_t t = s_sel[i];
       const int32_t s = s_slot[i];
       if (s >= 0) {
-        stp[s] = step;
+        for (int l = 0; l < nl; ++l) stp[(size_t)l * (size_t)a.meta_layer_slots + s] = step;
         if (out) out[i] = s;
       } else if (t < 0) {
         if (out) out[i] = -1;
       } else {
         const int32_t v = victim_of(i, t);
         const int32_t u = s_stok[v];
-        if (u >= 0) {
-          t2s[u] = -1;
-          ++nevict;
+        if (u >= 0) ++nevict;
+        for (int l = 0; l < nl; ++l) {
+          int32_t* t2s_l = t2s + (size_t)l * (size_t)a.meta_layer_ctx;
+          const size_t sl = (size_t)l * (size_t)a.meta_layer_slots;
+          if (u >= 0) t2s_l[u] = -1;
+          t2s_l[t] = v;
+          s2t[sl + v] = t;
+          stp[sl + v] = step;
         }
-        t2s[t] = v;
-        s2t[v] = t;
-        stp[v] = step;
         if (out) out[i] = v;
       }
     }
@@ -495,13 +511,16 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
 
   // counters
   nevict = __reduce_add_sync(0xffffffffu, nevict);
-  if (lane == 0 && nevict) atomicAdd(a.counters + 2, (unsigned long long)nevict);
+  if (lane == 0 && nevict)
+    for (int l = 0; l < nl; ++l) atomicAdd(a.counters + 4 * l + 2, (unsigned long long)nevict);
   if (rank == 0 && tid == 0) {
     int nv = 0;
     for (int w = 0; w < NW; ++w) nv += s_wval[w];
-    atomicAdd(a.counters + 0, (unsigned long long)(nv - m));
-    atomicAdd(a.counters + 1, (unsigned long long)m);
-    atomicAdd(a.counters + 3, (unsigned long long)m * (unsigned long long)R);
+    for (int l = 0; l < nl; ++l) {
+      atomicAdd(a.counters + 4 * l + 0, (unsigned long long)(nv - m));
+      atomicAdd(a.counters + 4 * l + 1, (unsigned long long)m);
+      atomicAdd(a.counters + 4 * l + 3, (unsigned long long)m * (unsigned long long)R);
+    }
   }
 }
 
@@ -678,9 +697,9 @@ int pick_cluster(const hs_pool* p, int batch) {
 }
 
 int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk, int32_t k, int32_t* out,
-                   cudaStream_t s) {
-  if (!p || layer < 0 || layer >= p->d.layers || batch < 0 || batch > p->d.max_batch || k < 0 ||
-      k > p->d.topk_max)
+                   cudaStream_t s, int32_t nlayers = 1) {
+  if (!p || layer < 0 || nlayers < 1 || layer > p->d.layers - nlayers || batch < 0 || batch > p->d.max_batch ||
+      k < 0 || k > p->d.topk_max)
     return HS_ERR_INVALID_ARG;
   if (batch == 0 || k == 0) return HS_OK;
   if (!topk) return HS_ERR_INVALID_ARG;
@@ -702,6 +721,11 @@ int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk
   a.slots = p->d.slots;
   a.row_bytes = p->d.row_bytes;
   a.cluster = pick_cluster(p, batch);
+  a.nlayers = nlayers;
+  a.meta_layer_ctx = (int64_t)p->d.max_batch * p->d.ctx;
+  a.meta_layer_slots = (int64_t)p->d.max_batch * p->d.slots;
+  a.src_layer_bytes = p->d.host_layer_stride;
+  a.hot_layer_bytes = (int64_t)p->d.max_batch * p->d.slots * p->d.row_bytes;
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
@@ -921,6 +945,13 @@ int hs_gather(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* out_sl
 int hs_gather_history(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* topk_idx, int32_t k, void* dst,
                       hs_stream_t stream) {
   return launch_gather(pool, layer, batch, topk_idx, k, dst, stream, true);
+}
+
+int hs_resolve_shared(hs_pool* pool, int32_t layer0, int32_t nlayers, int32_t batch, const int32_t* topk_idx,
+                      int32_t k, int32_t* out_slots, hs_stream_t stream) {
+  if (batch > 0 && k > 0 && !out_slots) return HS_ERR_INVALID_ARG;
+  return launch_resolve(pool, layer0, batch, topk_idx, k, out_slots, reinterpret_cast<cudaStream_t>(stream),
+                        nlayers);
 }
 
 int hs_get_error(hs_pool* pool, int32_t* out, int32_t clear) {

@@ -152,6 +152,18 @@ int hs_prefetch(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk
                 hs_stream_t stream);
 
 /*
+ * One resolve for `nlayers` consecutive layers layer0 .. layer0+nlayers-1 that share one selection per request
+ * (the models for which the HiSparse paper, Abstract, prefetches layer by layer). Layers that are always resolved
+ * together with the same selection hold identical metadata, so the victims are worked out once, from layer0, and
+ * every layer gets the same metadata update and its own rows (from its own part of the host pool) copied into its
+ * own hot buffer. The result -- state, counters, out_slots -- is exactly that of hs_resolve on each layer in turn.
+ * Precondition: the nlayers layers hold identical metadata (true when they have only ever been resolved through
+ * this call, or with identical selections). Arguments as hs_resolve; 1 <= nlayers, layer0 + nlayers <= layers.
+ */
+int hs_resolve_shared(hs_pool *pool, int32_t layer0, int32_t nlayers, int32_t batch, const int32_t *topk_idx,
+                      int32_t k, int32_t *out_slots, hs_stream_t stream);
+
+/*
  * The read a sparse-attention kernel makes after a resolve: for every request b < batch and entry i < k, copy hot
  * row out_slots[b][i] of `layer` to dst + (b*k + i)*row_bytes (a zero row for -1). dst: device memory of
  * batch*k*row_bytes bytes, 16-byte aligned. Enqueued on `stream`. Together with hs_gather_history it shows that

@@ -196,3 +196,40 @@ def test_argument_errors():
         hs.hs_pool_create(d)
     assert e.value.code == hs.HS_ERR_INVALID_ARG
     buf.close()
+
+
+@pytest.mark.parametrize("batch", [3, 40])
+def test_resolve_shared_small_and_ragged(batch):
+    # layers 1..3 resolved together with one selection, layer 0 and 4 on their own; small miss counts leave
+    # fewer blocks than first-wave warps
+    rng = np.random.default_rng(21 + batch)
+    ctx, slots, k, R = 3000, 200, 60, 48
+    L = 5
+    buf = _pool(L, batch, ctx, slots, k, R, seed=3)
+    ora = oracle.OraclePool(ctx, slots, R, L, batch, track_rows=False)
+    stream = torch.cuda.Stream()
+    prev = None
+    for step in range(10):
+        prev = _rand_sel(rng, batch, k, ctx, prev, keep=0.0 if step == 5 else 0.7, pad=0.05)
+        other = _rand_sel(rng, batch, k, ctx, None)
+        t = torch.from_numpy(prev).cuda()
+        t2 = torch.from_numpy(other).cuda()
+        outs = torch.full((L, batch, k), -9, dtype=torch.int32, device="cuda")
+        with torch.cuda.stream(stream):
+            hs.hs_step_begin(buf.handle, stream)
+            hs.hs_resolve(buf.handle, 0, batch, t2, k, outs[0], stream)
+            hs.hs_resolve_shared(buf.handle, 1, 3, batch, t, k, outs[1], stream)
+            hs.hs_resolve(buf.handle, 4, batch, t2, k, outs[4], stream)
+        stream.synchronize()
+        ora.step_begin()
+        assert np.array_equal(outs[0].cpu().numpy(), ora.resolve(0, other, None))
+        for l in (1, 2, 3):
+            assert np.array_equal(outs[1].cpu().numpy(), ora.resolve(l, prev, None)), (step, l)
+        assert np.array_equal(outs[4].cpu().numpy(), ora.resolve(4, other, None))
+    for name, ref in (("tok2slot", ora.tok2slot), ("slot_tok", ora.slot_tok), ("slot_stamp", ora.slot_stamp)):
+        assert np.array_equal(buf.view(name).cpu().numpy(), ref), name
+    assert np.array_equal(buf.view("counters").cpu().numpy().astype(np.uint64), ora.counters)
+    _check_rows(buf)
+    with pytest.raises(hs.HsError):
+        hs.hs_resolve_shared(buf.handle, 3, 3, batch, t, k, outs[0])  # past the last layer
+    buf.close()

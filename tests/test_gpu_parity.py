@@ -69,3 +69,12 @@ def test_shared_prefetch_in_graph():
     buf, _ = gh.replay(w, steps=4, prefetch=True, graphs=True)
     gh.check_hot_rows(buf, layers=[0, 1, 77])
     buf.close()
+
+
+def test_shared_selection_one_call_for_all_layers():
+    # hs_resolve_shared: one resolve per step drives all 78 layers; state, counters and rows equal the oracle's
+    # per-layer resolves
+    w = wl.WORKLOADS["shared"]
+    buf, _ = gh.replay(w, steps=12, shared_call=True)
+    gh.check_hot_rows(buf, layers=[0, 1, 40, 77])
+    buf.close()
