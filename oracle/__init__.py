@@ -51,6 +51,8 @@ def load_library(path: str):
     lib.ora_resolve_rl.restype = ctypes.c_int
     lib.ora_resolve_batch.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, vp, i32, vp, vp]
     lib.ora_resolve_batch.restype = ctypes.c_int
+    lib.ora_resolve_batch_tiered.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, vp, i32, vp, vp, vp]
+    lib.ora_resolve_batch_tiered.restype = ctypes.c_int
     return lib
 
 
@@ -92,11 +94,13 @@ class OraclePool:
         self.step += 1
 
     def resolve(self, layer: int, sel: np.ndarray, host_rows: np.ndarray | None = None,
-                want_slots: bool = True) -> np.ndarray | None:
+                want_slots: bool = True, resident: np.ndarray | None = None) -> np.ndarray | None:
         """Resolve one call for oracle layer `layer` over its requests.
 
-        sel: int32 [n_requests][k]; host_rows: uint8 [n_requests][ctx][row_bytes] (needed when rows are tracked).
-        Returns out_slots int32 [n_requests][k] (or None when want_slots is False, the prefetch form).
+        sel: int32 [n_requests][k]; host_rows: uint8 [n_requests][ctx][row_bytes] (needed when rows are tracked);
+        resident: optional int32 [n_requests][ctx], the row of each token still held in the HBM KV pool (or -1),
+        for the three-tier variant. Returns out_slots int32 [n_requests][k] (or None when want_slots is False,
+        the prefetch form).
         """
         sel = np.ascontiguousarray(sel, dtype=np.int32)
         nb, k = sel.shape
@@ -109,11 +113,16 @@ class OraclePool:
                 raise ValueError("host rows [requests][ctx][row_bytes] are needed when rows are tracked")
             host_rows = np.ascontiguousarray(host_rows, dtype=np.uint8)
         cnt = np.zeros(4, dtype=np.uint64)
-        rc = self._lib.ora_resolve_batch(self.step, self.ctx, self.slots, self.row_bytes, nb,
-                                         _ptr(self.tok2slot[layer]), _ptr(self.slot_tok[layer]),
-                                         _ptr(self.slot_stamp[layer]), _ptr(hot),
-                                         _ptr(host_rows) if hot is not None else None,
-                                         self.ctx * self.row_bytes, _ptr(sel), k, _ptr(out), _ptr(cnt))
+        if resident is not None:
+            resident = np.ascontiguousarray(resident, dtype=np.int32)
+            if resident.shape != (nb, self.ctx):
+                raise ValueError("resident map must be [requests][ctx]")
+        rc = self._lib.ora_resolve_batch_tiered(self.step, self.ctx, self.slots, self.row_bytes, nb,
+                                                _ptr(self.tok2slot[layer]), _ptr(self.slot_tok[layer]),
+                                                _ptr(self.slot_stamp[layer]), _ptr(hot),
+                                                _ptr(host_rows) if hot is not None else None,
+                                                self.ctx * self.row_bytes, _ptr(sel), k, _ptr(resident),
+                                                _ptr(out), _ptr(cnt))
         if rc < 0:
             raise RuntimeError(f"oracle precondition failed ({rc})")
         self.error |= rc

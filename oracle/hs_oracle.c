@@ -21,6 +21,12 @@
  *   5. Output. out_slots[i] = tok2slot[t_i] in input order (-1 for padding). Counters: hits += k' - m,
  *      misses += m, evictions += #{u >= 0}, bytes += m * row_bytes (k' = non-padding entries).
  *
+ * Three-tier variant ("Hybrid HiSparse" knowledge card, Timeline: one fused pass resolves resident, hot and
+ * missing rows, the hot pages coming from ordinary KV blocks of the same memory pool). With a resident map, a
+ * selected token that is not in the hot buffer but still held in the ordinary HBM KV pool (resident[t] = its row
+ * there, >= 0) is served in place: it is neither a hit nor a miss, takes no slot, refreshes no stamp, and its
+ * out_slot is -2 - resident[t]. It counts under hits (nothing is fetched). A hot-buffer hit takes precedence.
+ *
  * The readings of points the paper leaves open (stamp = decode step number, ties by lowest slot, ascending-token
  * pairing, empties first, padding and rejection rules) are the ones listed in the design notes of this
  * repository. The code below follows the steps literally with library sorts (qsort); it is deliberately slow.
@@ -53,9 +59,10 @@ static int cmp_cand(const void *a, const void *b) {
  * counters: [hits, misses, evictions, bytes] accumulated. Returns 0, or an OR of ORA_ERR_* bits (row rejected),
  * -1 on allocation failure, -2 if k > slots.
  */
-int ora_resolve_rl(int32_t step, int32_t ctx, int32_t slots, int32_t row_bytes, int32_t *tok2slot,
-                   int32_t *slot_tok, int32_t *slot_stamp, uint8_t *hot, const uint8_t *host_rows,
-                   const int32_t *sel, int32_t k, int32_t *out_slots, uint64_t *counters) {
+int ora_resolve_rl_tiered(int32_t step, int32_t ctx, int32_t slots, int32_t row_bytes, int32_t *tok2slot,
+                          int32_t *slot_tok, int32_t *slot_stamp, uint8_t *hot, const uint8_t *host_rows,
+                          const int32_t *sel, int32_t k, const int32_t *resident, int32_t *out_slots,
+                          uint64_t *counters) {
   /* precondition: a selection never exceeds the cache (the library rejects k > slots before launching) */
   if (k > slots) return -2;
   /* 0. validation */
@@ -85,7 +92,7 @@ int ora_resolve_rl(int32_t step, int32_t ctx, int32_t slots, int32_t row_bytes, 
     free(sorted), free(in_sel), free(miss), free(cand);
     return -1;
   }
-  int32_t m = 0, hits = 0;
+  int32_t m = 0, hits = 0, inplace = 0;
   for (int32_t i = 0; i < k; ++i) {
     const int32_t t = sel[i];
     if (t < 0) continue;
@@ -94,6 +101,8 @@ int ora_resolve_rl(int32_t step, int32_t ctx, int32_t slots, int32_t row_bytes, 
       slot_stamp[s] = step;
       in_sel[s] = 1;
       ++hits;
+    } else if (resident && resident[t] >= 0) {
+      ++inplace; /* served in place from the HBM-resident tier */
     } else {
       miss[m++] = t;
     }
@@ -129,6 +138,10 @@ int ora_resolve_rl(int32_t step, int32_t ctx, int32_t slots, int32_t row_bytes, 
   /* 5. outputs in input order, counters */
   if (out_slots)
     for (int32_t i = 0; i < k; ++i) out_slots[i] = sel[i] < 0 ? -1 : tok2slot[sel[i]];
+  if (out_slots && resident)
+    for (int32_t i = 0; i < k; ++i)
+      if (sel[i] >= 0 && out_slots[i] < 0) out_slots[i] = -2 - resident[sel[i]];
+  counters[0] += (uint64_t)inplace;
   counters[0] += (uint64_t)hits;
   counters[1] += (uint64_t)m;
   counters[2] += (uint64_t)evictions;
@@ -138,24 +151,40 @@ int ora_resolve_rl(int32_t step, int32_t ctx, int32_t slots, int32_t row_bytes, 
   return 0;
 }
 
+int ora_resolve_rl(int32_t step, int32_t ctx, int32_t slots, int32_t row_bytes, int32_t *tok2slot,
+                   int32_t *slot_tok, int32_t *slot_stamp, uint8_t *hot, const uint8_t *host_rows,
+                   const int32_t *sel, int32_t k, int32_t *out_slots, uint64_t *counters) {
+  return ora_resolve_rl_tiered(step, ctx, slots, row_bytes, tok2slot, slot_tok, slot_stamp, hot, host_rows, sel, k,
+                               NULL, out_slots, counters);
+}
+
 /*
  * A batch of request-layers of one layer, laid out contiguously: tok2slot [nb][ctx], slot_tok/slot_stamp
  * [nb][slots], hot [nb][slots][row_bytes] (or NULL), host rows of request b at host + b*host_req_stride,
  * selections [nb][k], out_slots [nb][k] (or NULL). Returns the OR of all per-row error bits (or a negative code).
  */
-int ora_resolve_batch(int32_t step, int32_t ctx, int32_t slots, int32_t row_bytes, int32_t nb, int32_t *tok2slot,
-                      int32_t *slot_tok, int32_t *slot_stamp, uint8_t *hot, const uint8_t *host,
-                      int64_t host_req_stride, const int32_t *sel, int32_t k, int32_t *out_slots,
-                      uint64_t *counters) {
+int ora_resolve_batch_tiered(int32_t step, int32_t ctx, int32_t slots, int32_t row_bytes, int32_t nb,
+                             int32_t *tok2slot, int32_t *slot_tok, int32_t *slot_stamp, uint8_t *hot,
+                             const uint8_t *host, int64_t host_req_stride, const int32_t *sel, int32_t k,
+                             const int32_t *resident, int32_t *out_slots, uint64_t *counters) {
   int err = 0;
   for (int32_t b = 0; b < nb; ++b) {
-    int r = ora_resolve_rl(step, ctx, slots, row_bytes, tok2slot + (size_t)b * (size_t)ctx,
-                           slot_tok + (size_t)b * (size_t)slots, slot_stamp + (size_t)b * (size_t)slots,
-                           hot ? hot + (size_t)b * (size_t)slots * (size_t)row_bytes : NULL,
-                           host ? host + (size_t)b * (size_t)host_req_stride : NULL, sel + (size_t)b * (size_t)k, k,
-                           out_slots ? out_slots + (size_t)b * (size_t)k : NULL, counters);
+    int r = ora_resolve_rl_tiered(step, ctx, slots, row_bytes, tok2slot + (size_t)b * (size_t)ctx,
+                                  slot_tok + (size_t)b * (size_t)slots, slot_stamp + (size_t)b * (size_t)slots,
+                                  hot ? hot + (size_t)b * (size_t)slots * (size_t)row_bytes : NULL,
+                                  host ? host + (size_t)b * (size_t)host_req_stride : NULL,
+                                  sel + (size_t)b * (size_t)k, k, resident ? resident + (size_t)b * (size_t)ctx : NULL,
+                                  out_slots ? out_slots + (size_t)b * (size_t)k : NULL, counters);
     if (r < 0) return r;
     err |= r;
   }
   return err;
+}
+
+int ora_resolve_batch(int32_t step, int32_t ctx, int32_t slots, int32_t row_bytes, int32_t nb, int32_t *tok2slot,
+                      int32_t *slot_tok, int32_t *slot_stamp, uint8_t *hot, const uint8_t *host,
+                      int64_t host_req_stride, const int32_t *sel, int32_t k, int32_t *out_slots,
+                      uint64_t *counters) {
+  return ora_resolve_batch_tiered(step, ctx, slots, row_bytes, nb, tok2slot, slot_tok, slot_stamp, hot, host,
+                                  host_req_stride, sel, k, NULL, out_slots, counters);
 }

@@ -37,15 +37,20 @@ def _rows(ctx, row_bytes, seed):
 # P1: brute force on tiny inputs. The victim set is found by exhaustive search over all subsets of the candidate
 # slots: the unique size-m subset whose every key is smaller than every key outside it.
 # ---------------------------------------------------------------------------------------------------------------
-def brute_force_step(tok2slot, slot_tok, stamp, sel, step):
-    """Advance plain-Python state (lists) by one call; returns (out_slots, hits, misses, evictions, fills)."""
+def brute_force_step(tok2slot, slot_tok, stamp, sel, step, resident=None):
+    """Advance plain-Python state (lists) by one call; returns (out_slots, hits, misses, evictions, fills).
+    With a resident map, a token outside the hot buffer but held in the HBM pool is served in place (counted as a
+    hit, out_slot -2 - row, no slot, no stamp)."""
     sel = [int(t) for t in sel]
     valid = [t for t in sel if t >= 0]
     hit_slots = set()
     misses = []
+    inplace = 0
     for t in valid:
         if tok2slot[t] >= 0:
             hit_slots.add(tok2slot[t])
+        elif resident is not None and resident[t] >= 0:
+            inplace += 1
         else:
             misses.append(t)
     for v in hit_slots:
@@ -74,6 +79,8 @@ def brute_force_step(tok2slot, slot_tok, stamp, sel, step):
         stamp[v] = step
         fills.append((t, v))
     out = [tok2slot[t] if t >= 0 else -1 for t in sel]
+    if resident is not None:
+        out = [(-2 - int(resident[t])) if (t >= 0 and o < 0) else o for t, o in zip(sel, out)]
     return out, len(valid) - m, m, evictions, fills
 
 
@@ -112,6 +119,67 @@ def pin_brute_force(lib, n_traces=300, seed=1):
             assert pool.slot_stamp[0, 0].tolist() == st, (trace, call)
             assert all(pool.hot[0, 0, v].tobytes() == hot[v] for v in range(slots)), (trace, call)
             assert pool.counters[0].tolist() == cnt.tolist(), (trace, call)
+
+
+def pin_brute_force_tiered(lib, n_traces=200, seed=11):
+    """The three-tier variant against the brute force, with a fresh random resident map for every call."""
+    rng = np.random.default_rng(seed)
+    for trace in range(n_traces):
+        ctx = int(rng.integers(4, 17))
+        slots = int(rng.integers(1, 9))
+        R = 8
+        rows = _rows(ctx, R, 5000 + trace)
+        pool = _pool(lib, ctx, slots, R)
+        t2s, s2t, st = [-1] * ctx, [-1] * slots, [0] * slots
+        hot = [bytes(R)] * slots
+        cnt = np.zeros(4, dtype=np.uint64)
+        step = 0
+        for call in range(int(rng.integers(2, 14))):
+            if call == 0 or rng.random() < 0.75:
+                pool.step_begin()
+                step += 1
+            k = int(rng.integers(1, min(slots, ctx) + 1))
+            sel = rng.choice(ctx, size=k, replace=False).astype(np.int32)
+            resident = np.where(rng.random(ctx) < 0.4, rng.integers(0, 1000, size=ctx), -1).astype(np.int32)
+            out_o = pool.resolve(0, sel[None, :], rows[None], resident=resident[None, :])
+            out_b, h, m, e, fills = brute_force_step(t2s, s2t, st, sel, step, resident)
+            for t, v in fills:
+                hot[v] = rows[t].tobytes()
+            cnt += np.array([h, m, e, m * R], dtype=np.uint64)
+            assert out_o[0].tolist() == out_b, (trace, call)
+            assert pool.tok2slot[0, 0].tolist() == t2s, (trace, call)
+            assert pool.slot_tok[0, 0].tolist() == s2t, (trace, call)
+            assert pool.slot_stamp[0, 0].tolist() == st, (trace, call)
+            assert all(pool.hot[0, 0, v].tobytes() == hot[v] for v in range(slots)), (trace, call)
+            assert pool.counters[0].tolist() == cnt.tolist(), (trace, call)
+
+
+def pin_tiered_all_resident(lib, seed=12):
+    """Closed form: when every selected token outside the hot buffer is held in the HBM pool, nothing is
+    fetched, no slot changes, and each such entry reports -2 - its pool row."""
+    rng = np.random.default_rng(seed)
+    ctx, slots, R = 500, 40, 8
+    rows = _rows(ctx, R, 9)
+    pool = _pool(lib, ctx, slots, R)
+    first = rng.choice(ctx, size=30, replace=False).astype(np.int32)
+    pool.step_begin()
+    pool.resolve(0, first[None, :], rows[None])
+    snap = (pool.tok2slot.copy(), pool.slot_tok.copy(), pool.slot_stamp.copy(), pool.hot.copy())
+    resident = np.arange(ctx, dtype=np.int32) * 3 + 1
+    sel = np.setdiff1d(rng.choice(ctx, size=60, replace=False), first)[:25].astype(np.int32)
+    c0 = pool.counters[0].copy()
+    pool.step_begin()
+    out = pool.resolve(0, sel[None, :], rows[None], resident=resident[None, :])
+    assert out[0].tolist() == (-2 - resident[sel]).tolist()
+    for a, b in zip(snap, (pool.tok2slot, pool.slot_tok, pool.slot_stamp, pool.hot)):
+        assert np.array_equal(a, b)
+    assert (pool.counters[0] - c0).tolist() == [len(sel), 0, 0, 0]
+    # a hot-buffer copy takes precedence over the resident one, and is re-stamped
+    both = first[:5]
+    pool.step_begin()
+    out = pool.resolve(0, both[None, :], rows[None], resident=resident[None, :])
+    assert np.array_equal(out[0], pool.tok2slot[0, 0][both])
+    assert np.all(pool.slot_stamp[0, 0][out[0]] == pool.step)
 
 
 # ---------------------------------------------------------------------------------------------------------------
@@ -296,4 +364,4 @@ def check_invariants(pool, layer, req, sel, out, host_rows, step, before, misses
 
 
 ALL_PINS = [pin_hand_trace, pin_rejection, pin_brute_force, pin_textbook_lru, pin_no_eviction_closed_form,
-            pin_churn_closed_form]
+            pin_churn_closed_form, pin_brute_force_tiered, pin_tiered_all_resident]

@@ -26,6 +26,11 @@ MUTANTS = [
     ("hits_miscounted", "counters[0] += (uint64_t)hits;", "counters[0] += (uint64_t)m;"),
     ("evictions_miscounted", "      ++evictions;\n", "\n"),
     ("range_check_off_by_one", "if (sel[i] >= ctx) err |= ORA_ERR_RANGE;", "if (sel[i] > ctx) err |= ORA_ERR_RANGE;"),
+    ("resident_fetched_anyway", "      ++inplace; /* served in place from the HBM-resident tier */",
+     "      miss[m++] = t;"),
+    ("resident_before_hot", "    if (s >= 0) {\n      slot_stamp[s] = step;\n      in_sel[s] = 1;\n      ++hits;\n    } else if",
+     "    if (s >= 0 && !(resident && resident[t] >= 0)) {\n      slot_stamp[s] = step;\n      in_sel[s] = 1;\n      ++hits;\n    } else if"),
+    ("resident_encoding_off_by_one", "out_slots[i] = -2 - resident[sel[i]];", "out_slots[i] = -1 - resident[sel[i]];"),
 ]
 
 

@@ -25,3 +25,11 @@ def test_no_eviction_closed_form():
 
 def test_full_churn_closed_form():
     pins.pin_churn_closed_form(None)
+
+
+def test_three_tier_brute_force():
+    pins.pin_brute_force_tiered(None)
+
+
+def test_three_tier_all_resident_closed_form():
+    pins.pin_tiered_all_resident(None)
