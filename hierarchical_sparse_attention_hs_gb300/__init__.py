@@ -21,7 +21,7 @@ __all__ = [
     "hs_pool_reset", "hs_step_begin", "hs_resolve", "hs_prefetch", "hs_get_error", "hs_get_counters",
     "hs_pool_destroy", "hs_host_alloc", "hs_host_free", "hs_error_string", "HS_DEVERR_RANGE", "HS_DEVERR_DUP",
     "HS_DEVERR_STATE", "HostBuffer", "PoolBuffers", "hs_probe_link", "hs_gather", "hs_gather_history",
-    "hs_resolve_shared",
+    "hs_resolve_shared", "hs_resolve_tiered",
 ]
 
 HS_OK = 0
@@ -79,6 +79,7 @@ def load():
             "hs_prefetch": (ctypes.c_int, [vp, i32, i32, vp, i32, vp]),
             "hs_gather": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp]),
             "hs_resolve_shared": (ctypes.c_int, [vp, i32, i32, i32, vp, i32, vp, vp]),
+            "hs_resolve_tiered": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, ctypes.c_int64, vp, vp]),
             "hs_gather_history": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp]),
             "hs_get_error": (ctypes.c_int, [vp, P(i32), i32]),
             "hs_get_counters": (ctypes.c_int, [vp, i32, P(ctypes.c_uint64)]),
@@ -168,6 +169,12 @@ def hs_resolve_shared(pool: int, layer0: int, nlayers: int, batch: int, topk_idx
                       stream=None) -> None:
     _check(load().hs_resolve_shared(pool, layer0, nlayers, batch, _addr(topk_idx), k, _addr(out_slots),
                                     _stream(stream)), "hs_resolve_shared")
+
+
+def hs_resolve_tiered(pool: int, layer: int, batch: int, topk_idx, k: int, resident_row, resident_stride: int,
+                      out_slots, stream=None) -> None:
+    _check(load().hs_resolve_tiered(pool, layer, batch, _addr(topk_idx), k, _addr(resident_row), resident_stride,
+                                    _addr(out_slots), _stream(stream)), "hs_resolve_tiered")
 
 
 def hs_gather(pool: int, layer: int, batch: int, out_slots, k: int, dst, stream=None) -> None:

@@ -62,7 +62,7 @@ constexpr int MAX_CLUSTER = 8;
 constexpr int GA_WARPS = NW / 2;                 // group A: miss ranks and the first wave of row loads
 constexpr int GA_THREADS = GA_WARPS * 32;
 constexpr int BITMAP_MAX_CTX = 1 << 18;          // longer contexts rank misses with the radix sort
-constexpr int MISC_BAD = 0, MISC_NCAND = 1, MISC_CBUF = 2, MISC_NEXT = 3, MISC_INTS = 4;
+constexpr int MISC_BAD = 0, MISC_NCAND = 1, MISC_CBUF = 2, MISC_NEXT = 3, MISC_NINP = 4, MISC_INTS = 5;
 
 struct ResolveArgs {
   const int32_t* topk;           // [batch][k]
@@ -80,6 +80,10 @@ struct ResolveArgs {
   int32_t cluster;               // CTAs per request-layer
   // Layers resolved by this launch: layer 0 of the args and the nlayers - 1 after it, whose caches hold the same
   // metadata (they are always resolved together with one shared selection). Strides between layers.
+  // Three-tier variant: row of each token still held in the ordinary HBM KV pool (>= 0) or -1, for request b at
+  // resident + b * resident_stride; nullptr when there is no such tier.
+  const int32_t* resident;
+  int64_t resident_stride;
   int32_t nlayers;
   int64_t meta_layer_ctx;        // int32 elements between layers in tok2slot
   int64_t meta_layer_slots;      // int32 elements between layers in slot_tok / slot_stamp
@@ -207,6 +211,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   const int32_t* sel = a.topk + (size_t)b * k;
   int32_t* out = a.out_slots ? a.out_slots + (size_t)b * k : nullptr;
   const uint8_t* src = a.src + (size_t)b * (size_t)a.src_req_stride;
+  const int32_t* res = a.resident ? a.resident + (size_t)b * (size_t)a.resident_stride : nullptr;
   uint8_t* hot = a.hot + (size_t)b * (size_t)H * (size_t)R;
   const int hwords = (H + 31) >> 5;
   const int cwords = (ctx + 31) >> 5;
@@ -268,12 +273,14 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   // 2. hit test over this warp's run of entries: hits mark their slot, misses their token
   int nvalid = 0, nmiss = 0;
   for (int i0 = wbeg; i0 < wend; i0 += 4 * 32) {
-    int32_t t[4], s[4];
+    int32_t t[4], s[4], r[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * 32 + lane;
       t[u] = i < wend ? s_sel[i] : -1;
-      s[u] = (t[u] >= 0 && t[u] < ctx) ? __ldcg(t2s + t[u]) : -1;
+      const bool ok = t[u] >= 0 && t[u] < ctx;
+      s[u] = ok ? __ldcg(t2s + t[u]) : -1;
+      r[u] = (ok && res) ? __ldcg(res + t[u]) : -1;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -284,11 +291,21 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
         bad |= HS_DEVERR_STATE;
         sl = -1;
       }
+      if (sl < 0 && r[u] >= 0) sl = -2 - r[u];  // served in place from the HBM-resident tier
       s_slot[i] = sl;
       if (sl >= 0) {
         const uint32_t bit = 1u << (sl & 31);
         if (atomicOr(&s_hit[sl >> 5], bit) & bit) bad |= HS_DEVERR_DUP;
-      } else if (t[u] >= 0 && t[u] < ctx) {
+      } else if (sl <= -2) {
+        // a repeated in-place token is caught here (bitmap; the bit is cleared again in step 3) or by a sort
+        // of the in-place list, kept at the top of s_mpos (radix)
+        if (BITMAP) {
+          const uint32_t bit = 1u << (t[u] & 31);
+          if (atomicOr(&s_bits[t[u] >> 5], bit) & bit) bad |= HS_DEVERR_DUP;
+        } else {
+          s_mpos[k - 1 - atomicAdd(&s_misc[MISC_NINP], 1)] = (uint16_t)i;
+        }
+      } else if (sl == -1 && t[u] >= 0 && t[u] < ctx) {
         if (BITMAP) {
           const uint32_t bit = 1u << (t[u] & 31);
           if (atomicOr(&s_bits[t[u] >> 5], bit) & bit) bad |= HS_DEVERR_DUP;
@@ -317,7 +334,8 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   }
   for (int base = wbeg; base < wend; base += 32) {
     const int i = base + lane;
-    const bool f = i < wend && s_slot[i] < 0 && s_sel[i] >= 0 && s_sel[i] < ctx;
+    const bool f = i < wend && s_slot[i] == -1 && s_sel[i] >= 0 && s_sel[i] < ctx;
+    if (BITMAP && i < wend && s_slot[i] <= -2) atomicAnd(&s_bits[s_sel[i] >> 5], ~(1u << (s_sel[i] & 31)));
     const unsigned bal = __ballot_sync(0xffffffffu, f);
     if (f) s_mpos[run + __popc(bal & hs::lanemask_lt())] = (uint16_t)i;
     run += __popc(bal);
@@ -382,6 +400,17 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
         s_rank[pos] = (uint16_t)j;
         if (j && s_sel[pos] == s_sel[s_mpos[order[j - 1]]]) bad |= HS_DEVERR_DUP;
       }
+    }
+    if (!BITMAP && s_misc[MISC_NINP] > 1) {
+      // repeated in-place tokens: sort the in-place list by token and compare neighbours
+      const int ninp = s_misc[MISC_NINP];
+      auto inp_tok = [&](int q) { return s_sel[s_mpos[k - 1 - q]]; };
+      g.sync();  // the miss ranking no longer reads the sort buffers
+      int n2 = 0;
+      const uint16_t* order = hs::radix_sort(g, ninp, bits_of((unsigned)(ctx - 1)), s_mbuf, s_mbuf + k, inp_tok,
+                                             [](int) { return true; }, s_tbl, red, &n2);
+      for (int j = g.tid() + 1; j < ninp; j += GA_THREADS)
+        if (inp_tok(order[j]) == inp_tok(order[j - 1])) bad |= HS_DEVERR_DUP;
     }
     if (tid == 0) s_misc[MISC_NEXT] = min(GA_WARPS, my_blocks);  // the first wave took blocks [0, this)
   } else {
@@ -480,8 +509,8 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
       if (s >= 0) {
         for (int l = 0; l < nl; ++l) stp[(size_t)l * (size_t)a.meta_layer_slots + s] = step;
         if (out) out[i] = s;
-      } else if (t < 0) {
-        if (out) out[i] = -1;
+      } else if (t < 0 || s <= -2) {
+        if (out) out[i] = t < 0 ? -1 : s;  // padding, or a row served in place (-2 - its pool row)
       } else {
         const int32_t v = victim_of(i, t);
         const int32_t u = s_stok[v];
@@ -697,7 +726,8 @@ int pick_cluster(const hs_pool* p, int batch) {
 }
 
 int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk, int32_t k, int32_t* out,
-                   cudaStream_t s, int32_t nlayers = 1) {
+                   cudaStream_t s, int32_t nlayers = 1, const int32_t* resident = nullptr,
+                   int64_t resident_stride = 0) {
   if (!p || layer < 0 || nlayers < 1 || layer > p->d.layers - nlayers || batch < 0 || batch > p->d.max_batch ||
       k < 0 || k > p->d.topk_max)
     return HS_ERR_INVALID_ARG;
@@ -722,6 +752,8 @@ int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk
   a.row_bytes = p->d.row_bytes;
   a.cluster = pick_cluster(p, batch);
   a.nlayers = nlayers;
+  a.resident = resident;
+  a.resident_stride = resident_stride;
   a.meta_layer_ctx = (int64_t)p->d.max_batch * p->d.ctx;
   a.meta_layer_slots = (int64_t)p->d.max_batch * p->d.slots;
   a.src_layer_bytes = p->d.host_layer_stride;
@@ -952,6 +984,15 @@ int hs_resolve_shared(hs_pool* pool, int32_t layer0, int32_t nlayers, int32_t ba
   if (batch > 0 && k > 0 && !out_slots) return HS_ERR_INVALID_ARG;
   return launch_resolve(pool, layer0, batch, topk_idx, k, out_slots, reinterpret_cast<cudaStream_t>(stream),
                         nlayers);
+}
+
+int hs_resolve_tiered(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* topk_idx, int32_t k,
+                      const int32_t* resident_row, int64_t resident_stride, int32_t* out_slots,
+                      hs_stream_t stream) {
+  if (batch > 0 && k > 0 && (!out_slots || !resident_row)) return HS_ERR_INVALID_ARG;
+  if (!pool || resident_stride < (int64_t)pool->d.ctx) return HS_ERR_INVALID_ARG;
+  return launch_resolve(pool, layer, batch, topk_idx, k, out_slots, reinterpret_cast<cudaStream_t>(stream), 1,
+                        resident_row, resident_stride);
 }
 
 int hs_get_error(hs_pool* pool, int32_t* out, int32_t clear) {

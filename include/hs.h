@@ -164,6 +164,18 @@ int hs_resolve_shared(hs_pool *pool, int32_t layer0, int32_t nlayers, int32_t ba
                       int32_t k, int32_t *out_slots, hs_stream_t stream);
 
 /*
+ * Three-tier variant ("Hybrid HiSparse" knowledge card, Timeline: resident, hot and missing rows resolved in one
+ * fused pass; hot pages come from ordinary KV blocks of the same memory pool). resident_row: device int32, for
+ * request b at resident_row + b*resident_stride (resident_stride >= ctx), the row of each token still held in
+ * the ordinary HBM KV pool (0 <= row <= 2^31 - 3), or -1. A selected token that is not in the hot buffer but is
+ * resident there is served in place: it takes no slot, refreshes no stamp, is fetched from nowhere, counts as a
+ * hit, and its out_slot is -2 - row. A hot-buffer hit takes precedence. Everything else is as hs_resolve.
+ */
+int hs_resolve_tiered(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk_idx, int32_t k,
+                      const int32_t *resident_row, int64_t resident_stride, int32_t *out_slots,
+                      hs_stream_t stream);
+
+/*
  * The read a sparse-attention kernel makes after a resolve: for every request b < batch and entry i < k, copy hot
  * row out_slots[b][i] of `layer` to dst + (b*k + i)*row_bytes (a zero row for -1). dst: device memory of
  * batch*k*row_bytes bytes, 16-byte aligned. Enqueued on `stream`. Together with hs_gather_history it shows that

@@ -190,3 +190,29 @@ def xoshiro_sequence(state, n: int) -> np.ndarray:
     out = np.empty(n, dtype=np.uint64)
     _load().wl_xoshiro_sequence(*[ctypes.c_uint64(s) for s in state], n, out.ctypes.data)
     return out
+
+
+def gen_resident(ctx: int, batch: int, steps: int, seed: int, window: int = 256, page: int = 64,
+                 frac: float = 0.3) -> np.ndarray:
+    """Resident-tier maps int32 [steps][batch][ctx] for the three-tier resolver: entry t is the row of token t in
+    the ordinary HBM KV pool, or -1 when the token's KV lives only in host memory.
+
+    Recipe: the newest `window` tokens are resident (they were written by the latest decode steps), and every
+    other page of `page` tokens is resident with probability `frac`, drawn afresh each step. Resident pages take
+    distinct pool blocks in random order, so rows are distinct within a request.
+    """
+    if ctx % page:
+        raise ValueError("ctx must be a multiple of page")
+    rng = np.random.default_rng([seed, 0x5E5D, ctx, batch])
+    npages = ctx // page
+    out = np.full((steps, batch, ctx), -1, dtype=np.int32)
+    first_window_page = max(0, (ctx - window) // page)
+    for s in range(steps):
+        for b in range(batch):
+            res = rng.random(npages) < frac
+            res[first_window_page:] = True
+            pages = np.flatnonzero(res)
+            blocks = rng.permutation(npages)[: len(pages)]
+            rows = (blocks[:, None] * page + np.arange(page)[None, :]).astype(np.int32)
+            out[s, b].reshape(npages, page)[pages] = rows
+    return out
