@@ -144,6 +144,18 @@ __device__ __forceinline__ uint4 load_row_chunk(const uint8_t* p) {
   return FROM_HOST ? load_row_chunk_host(p) : load_row_chunk_device(p);
 }
 
+// Asynchronous global-to-shared copies (completion waited for by the issuing thread, then a block barrier).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Every warp executes these as a whole (the .aligned forms).
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -225,62 +237,54 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   const int wbeg = min(k, warp * wseg);
   const int wend = min(k, wbeg + wseg);
 
-  // 1. selection row, slot metadata, empty bitmaps, per-warp stamp range
+  // 1. the slot metadata starts on its way to shared memory (asynchronous copies, waited for at the end of step
+  //    2), the first entries of this warp's run of the selection are loaded, and the bitmaps are cleared
   unsigned bad = 0;
+  if ((H & 3) == 0) {  // per-request arrays start on 16-byte boundaries
+    for (int c = tid; c < (H >> 2); c += NT) {
+      cp_async16(s_stamp + 4 * c, stp + 4 * c);
+      cp_async16(s_stok + 4 * c, s2t + 4 * c);
+    }
+  } else {
+    for (int v = tid; v < H; v += NT) {
+      cp_async4(s_stamp + v, stp + v);
+      cp_async4(s_stok + v, s2t + v);
+    }
+  }
+  cp_async_commit();
+  constexpr int RUN_STEP = 4 * 32;  // entries of a warp's run per iteration
+  int32_t tn[4];
+  auto load_sel = [&](int i0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * 32 + lane;
+      tn[u] = i < wend ? __ldcg(sel + i) : -1;
+    }
+  };
+  load_sel(wbeg);
   if (tid < MISC_INTS) s_misc[tid] = 0;
-  for (int i0 = tid; i0 < k; i0 += 4 * NT) {
-    int32_t t[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) t[u] = i0 + u * NT < k ? __ldcg(sel + i0 + u * NT) : 0;
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (i0 + u * NT < k) {
-        s_sel[i0 + u * NT] = t[u];
-        if (t[u] >= ctx) bad |= HS_DEVERR_RANGE;
-      }
-  }
-  int lo = 0x7fffffff, hi = -1;
-  for (int v0 = tid; v0 < H; v0 += 4 * NT) {
-    int32_t st[4], tk[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int v = v0 + u * NT;
-      st[u] = v < H ? __ldcg(stp + v) : 0;
-      tk[u] = v < H ? __ldcg(s2t + v) : 0;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int v = v0 + u * NT;
-      if (v < H) {
-        s_stamp[v] = st[u];
-        s_stok[v] = tk[u];
-        lo = min(lo, st[u]);
-        hi = max(hi, st[u]);
-      }
-    }
-  }
   for (int w = tid; w < hwords; w += NT) s_hit[w] = 0u;
   if (BITMAP)
     for (int w = tid; w < cwords; w += NT) s_bits[w] = 0u;
-  lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)lo);
-  hi = __reduce_max_sync(0xffffffffu, hi);
-  if (lane == 0) {
-    s_wlo[warp] = lo;
-    s_whi[warp] = hi;
-  }
   __syncthreads();
 
   // 2. hit test over this warp's run of entries: hits mark their slot, misses their token
   int nvalid = 0, nmiss = 0;
-  for (int i0 = wbeg; i0 < wend; i0 += 4 * 32) {
+  for (int i0 = wbeg; i0 < wend; i0 += RUN_STEP) {
     int32_t t[4], s[4], r[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) t[u] = tn[u];
+    if (i0 + RUN_STEP < wend) load_sel(i0 + RUN_STEP);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * 32 + lane;
-      t[u] = i < wend ? s_sel[i] : -1;
       const bool ok = t[u] >= 0 && t[u] < ctx;
       s[u] = ok ? __ldcg(t2s + t[u]) : -1;
       r[u] = (ok && res) ? __ldcg(res + t[u]) : -1;
+      if (i < wend) {
+        s_sel[i] = t[u];
+        if (t[u] >= ctx) bad |= HS_DEVERR_RANGE;
+      }
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -321,6 +325,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     s_wval[warp] = nvalid;
     s_wmiss[warp] = nmiss;
   }
+  cp_async_wait_all();
   __syncthreads();
   // Every read of the cluster-shared metadata by this CTA has completed.
   if (C > 1) cluster_arrive();
@@ -417,9 +422,22 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     // B: victims in (stamp, slot) order
     const Group g{GA_WARPS, NW - GA_WARPS, 2};
     int smin = 0x7fffffff, smax = -1;
-    for (int w = 0; w < NW; ++w) {
-      smin = min(smin, s_wlo[w]);
-      smax = max(smax, s_whi[w]);
+    if (m > 0) {
+      for (int v = g.tid(); v < H; v += g.size()) {
+        smin = min(smin, s_stamp[v]);
+        smax = max(smax, s_stamp[v]);
+      }
+      smin = (int)__reduce_min_sync(0xffffffffu, (unsigned)smin);
+      smax = __reduce_max_sync(0xffffffffu, smax);
+      if (lane == 0) {
+        s_wlo[g.warp()] = smin;
+        s_whi[g.warp()] = smax;
+      }
+      g.sync();
+      for (int w = 0; w < g.nw; ++w) {
+        smin = min(smin, s_wlo[w]);
+        smax = max(smax, s_whi[w]);
+      }
     }
     const int stamp_bits = smax >= smin ? bits_of((unsigned)(smax - smin)) : 0;
     int ncand = 0;
