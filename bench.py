@@ -162,7 +162,7 @@ class GpuRun:
 
     def __init__(self, w: wl.Workload, noio: bool = False, prefetch: bool = False, host: object = None,
                  host_layers: int | None = None, layer_work_mb: float = 0.0, work_only: bool = False,
-                 full_offload: bool = False, shared_call: bool = False):
+                 full_offload: bool = False, shared_call: bool = False, tiered_frac: float | None = None):
         import torch
 
         import hierarchical_sparse_attention_hs_gb300 as hs
@@ -194,6 +194,11 @@ class GpuRun:
         self.full_offload = full_offload
         # Layers that share one selection resolved by a single hs_resolve_shared call per step
         self.shared_call = shared_call and w.shared_across_layers
+        # Three-tier resolution: per step, a resident map of the tokens still held in the HBM KV pool (one map per
+        # request, shared by all layers as a block table is), kept in device memory like the pool's block table
+        self.res = None
+        if tiered_frac is not None:
+            self.res = torch.from_numpy(wl.gen_resident(w.ctx, w.requests, w.steps, w.seed, frac=tiered_frac)).cuda()
         if full_offload:
             self.offload_buf = torch.empty(w.requests * w.topk * w.row_bytes, dtype=torch.uint8, device="cuda")
         if self.layer_work:
@@ -241,6 +246,12 @@ class GpuRun:
         if self.shared_call:
             hs.hs_resolve_shared(self.pool, 0, w.layers, w.requests, src[0], w.topk, self.out[0], st)
             for l in range(w.layers):
+                self.enqueue_layer_work(l)
+            return
+        if self.res is not None:
+            for l in range(w.layers):
+                hs.hs_resolve_tiered(self.pool, l, w.requests, src[self._lsel(l)], w.topk, self.res[s], w.ctx,
+                                     self.out[l], st)
                 self.enqueue_layer_work(l)
             return
         if not self.prefetch:
@@ -376,27 +387,58 @@ def measure_link(hs, torch, host_ptr: int, nbytes: int, chunk: int = 1 << 30) ->
     return best_zc, best_cp
 
 
-def cpu_baseline(w: wl.Workload, budget_s: float = 12.0) -> dict:
-    """The CPU oracle, single-threaded, on a bounded sample of the same workload (request-layers of layer 0,
-    with hot rows tracked in host memory, steps in order from the cold start until the time budget)."""
+def _oracle_requests(w: wl.Workload, lo: int, hi: int, sel: np.ndarray, host: np.ndarray, res, budget_s: float,
+                     t0: float) -> tuple:
+    """Steps of layer 0 for requests lo..hi-1 from the cold start, the sequence replayed from a fresh cache each
+    time it ends (as the GPU passes do), until the budget; (selections, steps)."""
     import oracle
+
+    n = steps = 0
+    while time.perf_counter() - t0 < budget_s:
+        pool = oracle.OraclePool(w.ctx, w.slots, w.row_bytes, 1, hi - lo, track_rows=True)
+        for s in range(w.steps):
+            if time.perf_counter() - t0 >= budget_s:
+                break
+            pool.step_begin()
+            pool.resolve(0, sel[s, 0, lo:hi], host[lo:hi], resident=None if res is None else res[s, lo:hi])
+            n += hi - lo
+            steps += 1
+    return n, steps
+
+
+def cpu_baseline(w: wl.Workload, budget_s: float = 12.0, tiered_frac: float | None = None,
+                 threads: int = 1) -> dict:
+    """The CPU oracle on a bounded sample of the same workload: request-layers of layer 0, hot rows tracked in
+    host memory, steps in order from the cold start until the time budget. With threads > 1 the requests are
+    split over that many threads (the oracle's C routine runs without the interpreter lock), each resolving its
+    own requests, which are independent."""
+    import threading
 
     reqs = w.requests
     sel = wl.gen_selections(w, layers=(0, 1), requests=(0, reqs))
     host = np.stack([wl.rows(w, 0, b) for b in range(reqs)])
-    pool = oracle.OraclePool(w.ctx, w.slots, w.row_bytes, 1, reqs, track_rows=True)
+    res = None if tiered_frac is None else wl.gen_resident(w.ctx, reqs, w.steps, w.seed, frac=tiered_frac)
+    threads = max(1, min(threads, reqs))
+    bounds = [reqs * i // threads for i in range(threads + 1)]
+    results = [None] * threads
     t0 = time.perf_counter()
-    n = 0
-    s = 0
-    while s < w.steps and time.perf_counter() - t0 < budget_s:
-        pool.step_begin()
-        pool.resolve(0, sel[s, 0], host)
-        n += reqs
-        s += 1
+
+    def work(i):
+        results[i] = _oracle_requests(w, bounds[i], bounds[i + 1], sel, host, res, budget_s, t0)
+
+    ths = [threading.Thread(target=work, args=(i,)) for i in range(threads)]
+    for t in ths:
+        t.start()
+    for t in ths:
+        t.join()
     dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"layer 0 of {w.name}, {reqs} requests, steps 0..{s - 1} from the cold start ({n} selections, "
-                      f"hot rows tracked, {dt:.1f} s single-threaded)"}
+    n = sum(r[0] for r in results)
+    steps = min(r[1] for r in results)
+    mode = "single-threaded" if threads == 1 else f"{threads} threads over the requests"
+    return {"value": n / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"layer 0 of {w.name}, {reqs} requests, at least {steps} decode steps (the {w.steps}-step "
+                      f"sequence replayed from the cold start; {n} selections, hot rows tracked" +
+                      (", resident maps" if res is not None else "") + f", {dt:.1f} s {mode})"}
 
 
 def max_over_ranks(ms: float, dist=None) -> float:
@@ -490,7 +532,7 @@ def run_gpu(args) -> int:
     w = wl.WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
     run = GpuRun(w, prefetch=args.prefetch, layer_work_mb=args.layer_work_mb, work_only=args.work_only,
-                 full_offload=args.full_offload, shared_call=args.shared_call)
+                 full_offload=args.full_offload, shared_call=args.shared_call, tiered_frac=args.tiered_frac)
     # The GPU reads the whole host pool once (as a long-running server has long since done), so that first-touch
     # address translation of host pages is not charged to the timed steps; it also measures the link.
     link_zc, link_cp = measure_link(hs, torch, run.buf.host.ptr, run.buf.host.nbytes // 16 * 16)
@@ -524,6 +566,8 @@ def run_gpu(args) -> int:
         miss_bytes = misses * w.row_bytes
     link_peak = max(link_zc, link_cp)
     meta = n_launch * meta_bytes_per_launch(w, w.requests) + 4 * hits + 16 * misses
+    if run.res is not None:  # the resident-map lookup of every selected token
+        meta += 4 * n_launch * w.requests * w.topk
     hbm_bytes = meta + miss_bytes
     t_link = miss_bytes / (link_peak * 1e9)
     t_hbm = hbm_bytes / (hbm_peak * 1e9)
@@ -565,7 +609,7 @@ def run_gpu(args) -> int:
     if not args.skip_noio:
         nrun = GpuRun(w, noio=True, prefetch=args.prefetch, host=host, host_layers=run.host_layers,
                       layer_work_mb=args.layer_work_mb, work_only=args.work_only, full_offload=args.full_offload,
-                      shared_call=args.shared_call)
+                      shared_call=args.shared_call, tiered_frac=args.tiered_frac)
         nrun.run_steps(W, timed=False)
         nrun.reset()
         nper, _ = nrun.run_steps(K)
@@ -593,7 +637,8 @@ def run_gpu(args) -> int:
                                  "layers share one host pool (host_layer_stride 0); every miss still crosses the link"),
                    "graphs": "one CUDA graph per decode step", "prefetch": bool(args.prefetch),
                    "layer_work_mb": args.layer_work_mb, "work_only": bool(args.work_only),
-                   "full_offload": bool(args.full_offload), "shared_call": bool(args.shared_call)},
+                   "full_offload": bool(args.full_offload), "shared_call": bool(args.shared_call),
+                   "tiered_frac": args.tiered_frac},
         "selected_entries_per_s": value * w.topk,
         "miss_gbs": miss_bytes / (total_ms / 1e3) / 1e9 * world,
         "cold_step_ms": statistics.mean(cold) if cold else None,
@@ -606,7 +651,10 @@ def run_gpu(args) -> int:
         "clocks": clocks,
     }
     if rank == 0 and not args.skip_cpu:
-        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget, tiered_frac=args.tiered_frac)
+        if args.cpu_threads > 1:
+            line["cpu_baseline_threads"] = cpu_baseline(w, budget_s=args.cpu_budget, tiered_frac=args.tiered_frac,
+                                                        threads=args.cpu_threads)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -633,10 +681,18 @@ def main() -> int:
     ap.add_argument("--skip-noio", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-threads", type=int, default=os.cpu_count() or 1,
+                    help="threads of the second, multi-threaded CPU-oracle line (1 = skip it)")
+    ap.add_argument("--tiered-frac", type=float, default=None,
+                    help="three-tier resolution: fraction of pages still held in the HBM KV pool (plus the newest "
+                         "256 tokens), one resident map per request and step")
     ap.add_argument("--ref-layers", type=int, default=1, help="reference arm: layers resolved per step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.tiered_frac is not None and (args.prefetch or args.shared_call or args.full_offload):
+        ap.error("--tiered-frac resolves each layer with its own call; it combines with none of --prefetch, "
+                 "--shared-call, --full-offload")
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
