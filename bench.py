@@ -183,6 +183,7 @@ class GpuRun:
         self.out = torch.empty((w.layers, w.requests, w.topk), dtype=torch.int32, device="cuda")
         self.stream = torch.cuda.Stream()
         self.side = torch.cuda.Stream() if prefetch else None
+        self.host_io = None
         self.flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
         # Stand-in for the rest of a decoder layer, run after each layer's resolve on the main stream: the
         # sparse-attention read of the selected rows (hs_gather) plus a copy of layer_work_mb MB (the layer's
@@ -214,6 +215,21 @@ class GpuRun:
     def _lsel(self, l):
         return 0 if self.w.shared_across_layers else l
 
+    def _sel(self, s, ls):
+        """Selection rows of step s, selection layer ls: the device copy, or (while graphs for the zero-copy
+        end-to-end pass are captured) the address in the mapped host buffer."""
+        if self.host_io is None:
+            return self.sel[s][ls]
+        host_sel, _ = self.host_io
+        w = self.w
+        return host_sel.ptr + ((s * w.selection_layers + ls) * w.requests * w.topk) * 4
+
+    def _out(self, l):
+        if self.host_io is None:
+            return self.out[l]
+        _, host_out = self.host_io
+        return host_out.ptr + l * self.w.requests * self.w.topk * 4
+
     def enqueue(self, s):
         """Enqueue decode step s on self.stream: hs_step_begin, then the step's resolves."""
         if self.work_only:
@@ -223,7 +239,7 @@ class GpuRun:
         if self.full_offload:
             w = self.w
             for l in range(w.layers):
-                self.hs.hs_gather_history(self.pool, l, w.requests, self.sel[s][self._lsel(l)], w.topk,
+                self.hs.hs_gather_history(self.pool, l, w.requests, self._sel(s, self._lsel(l)), w.topk,
                                           self.offload_buf, self.stream)
             return
         self.hs.hs_step_begin(self.pool, self.stream)
@@ -233,7 +249,7 @@ class GpuRun:
         if not self.layer_work:
             return
         w = self.w
-        self.hs.hs_gather(self.pool, l, w.requests, self.out[l], w.topk, self.gather_buf, self.stream)
+        self.hs.hs_gather(self.pool, l, w.requests, self._out(l), w.topk, self.gather_buf, self.stream)
         with self.torch.cuda.stream(self.stream):
             self.work_dst.copy_(self.work_src)
 
@@ -242,21 +258,23 @@ class GpuRun:
         layer's work stand-in when there is one."""
         torch, hs, w = self.torch, self.hs, self.w
         st = self.stream
-        src = self.sel[s]
+        def src(ls):
+            return self._sel(s, ls)
+
         if self.shared_call:
-            hs.hs_resolve_shared(self.pool, 0, w.layers, w.requests, src[0], w.topk, self.out[0], st)
+            hs.hs_resolve_shared(self.pool, 0, w.layers, w.requests, src(0), w.topk, self._out(0), st)
             for l in range(w.layers):
                 self.enqueue_layer_work(l)
             return
         if self.res is not None:
             for l in range(w.layers):
-                hs.hs_resolve_tiered(self.pool, l, w.requests, src[self._lsel(l)], w.topk, self.res[s], w.ctx,
-                                     self.out[l], st)
+                hs.hs_resolve_tiered(self.pool, l, w.requests, src(self._lsel(l)), w.topk, self.res[s], w.ctx,
+                                     self._out(l), st)
                 self.enqueue_layer_work(l)
             return
         if not self.prefetch:
             for l in range(w.layers):
-                hs.hs_resolve(self.pool, l, w.requests, src[self._lsel(l)], w.topk, self.out[l], st)
+                hs.hs_resolve(self.pool, l, w.requests, src(self._lsel(l)), w.topk, self._out(l), st)
                 self.enqueue_layer_work(l)
             return
         # exact layer-wise prefetch: once layer l starts on the main stream, layer l+1 is resolved on the side
@@ -270,10 +288,10 @@ class GpuRun:
                 started = torch.cuda.Event()
                 started.record(st)
                 side.wait_event(started)
-                hs.hs_prefetch(self.pool, l + 1, w.requests, src[self._lsel(l + 1)], w.topk, side)
+                hs.hs_prefetch(self.pool, l + 1, w.requests, src(self._lsel(l + 1)), w.topk, side)
                 done[l + 1] = torch.cuda.Event()
                 done[l + 1].record(side)
-            hs.hs_resolve(self.pool, l, w.requests, src[self._lsel(l)], w.topk, self.out[l], st)
+            hs.hs_resolve(self.pool, l, w.requests, src(self._lsel(l)), w.topk, self._out(l), st)
             self.enqueue_layer_work(l)
 
     def _capture(self, s):
@@ -339,7 +357,57 @@ class GpuRun:
         return self.buf.view("counters").cpu().numpy().astype(np.int64).sum(axis=0)
 
     def e2e_pass(self, k_steps: int):
-        """Public-API loop with host buffers: per step, copy the selections in from pinned host memory, run the
+        """Public-API loop with host buffers, zero-copy: the step graphs are captured again with the selections
+        and out_slots in mapped page-locked host memory, which the kernels read and write over the host link
+        themselves; events bracket each whole step. Returns (ms, h2d bytes, d2h bytes, out_slots match)."""
+        torch, hs, w = self.torch, self.hs, self.w
+        host_sel = hs.HostBuffer(self.sel_host.nbytes)
+        host_out = hs.HostBuffer(self.out.numel() * 4)
+        np.frombuffer(host_sel.numpy(), dtype=np.int32)[:] = self.sel_host.reshape(-1)
+        self.host_io = (host_sel, host_out)
+        try:
+            graphs = [self._capture(s) for s in range(w.steps)]
+        finally:
+            self.host_io = None
+        torch.cuda.synchronize()
+        # first pass of the sequence on the device-memory graphs, kept for comparison with the zero-copy pass
+        self.reset()
+        ref = []
+        for pos in range(w.steps):
+            with torch.cuda.stream(self.stream):
+                self.graphs[pos].replay()
+            self.stream.synchronize()
+            ref.append(self.out.cpu().numpy().copy())
+        self.reset()
+        host_out_np = np.frombuffer(host_out.numpy(), dtype=np.int32).reshape(tuple(self.out.shape))
+        writes_slots = not (self.full_offload or self.work_only)
+        match = True if writes_slots else None
+        times = []
+        pos = 0
+        for _ in range(k_steps):
+            if pos == w.steps:
+                pos = 0
+                self.reset()
+            self.flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            with torch.cuda.stream(self.stream):
+                graphs[pos].replay()
+            e1.record(self.stream)
+            times.append((e0, e1))
+            e1.synchronize()
+            if writes_slots:
+                match = match and bool(np.array_equal(host_out_np, ref[pos]))
+            pos += 1
+        self.stream.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in times)
+        del graphs
+        host_sel.close()
+        host_out.close()
+        return ms, self.sel[0].numel() * 4, self.out.numel() * 4, match
+
+    def e2e_copy_pass(self, k_steps: int):
+        """The same loop with explicit copies: per step, copy the selections in from pinned host memory, run the
         step's graph, copy out_slots back to pinned host memory; events bracket the whole step."""
         torch = self.torch
         w = self.w
@@ -594,11 +662,20 @@ def run_gpu(args) -> int:
                        f"HBM {hbm_peak:.1f} GB/s {hbm_src}",
     }
 
-    # end to end through the public API with host buffers
-    e2e_ms, h2d, d2h = run.e2e_pass(K)
+    # end to end through the public API with host buffers: zero-copy (the kernels read the selections from and
+    # write out_slots to mapped host memory), and with explicit staging copies
+    e2e_ms, h2d, d2h, e2e_match = run.e2e_pass(K)
     e2e_ms = max_over_ranks(e2e_ms, dist)
+    c_ms, c_h2d, c_d2h = run.e2e_copy_pass(K)
+    c_ms = max_over_ranks(c_ms, dist)
     e2e = {"value": aggregate_rate(world, K * sel_per_step, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h}
+           "d2h_bytes_per_step": d2h,
+           "path": "selections and out_slots in mapped page-locked host memory, read and written by the kernels "
+                   "over the host link (no staging copies); L2 flushed between steps",
+           "out_slots_match_device_path": e2e_match,
+           "with_copies": {"value": aggregate_rate(world, K * sel_per_step, c_ms), "unit": UNIT,
+                           "h2d_bytes_per_step": c_h2d, "d2h_bytes_per_step": c_d2h,
+                           "path": "cudaMemcpyAsync of the selections in and out_slots out around each step's graph"}}
     host = run.buf.host
     run.buf.host = None
     run.close()
@@ -652,7 +729,7 @@ def run_gpu(args) -> int:
     }
     if rank == 0 and not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget, tiered_frac=args.tiered_frac)
-        if args.cpu_threads > 1:
+        if min(args.cpu_threads, w.requests) > 1:
             line["cpu_baseline_threads"] = cpu_baseline(w, budget_s=args.cpu_budget, tiered_frac=args.tiered_frac,
                                                         threads=args.cpu_threads)
     if rank == 0:

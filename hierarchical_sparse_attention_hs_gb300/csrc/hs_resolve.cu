@@ -144,6 +144,15 @@ __device__ __forceinline__ uint4 load_row_chunk(const uint8_t* p) {
   return FROM_HOST ? load_row_chunk_host(p) : load_row_chunk_device(p);
 }
 
+// Loads of the caller's index arrays (selections, resident maps, slot lists): `.cv` fetches afresh, so a stale
+// L2 copy of a host-memory line is never used and these arrays may live in device memory or in mapped
+// page-locked host memory, read over the host link without a separate copy.
+__device__ __forceinline__ int32_t ld_fresh(const int32_t* p) {
+  int32_t v;
+  asm("ld.global.cv.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 // Asynchronous global-to-shared copies (completion waited for by the issuing thread, then a block barrier).
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
@@ -258,7 +267,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * 32 + lane;
-      tn[u] = i < wend ? __ldcg(sel + i) : -1;
+      tn[u] = i < wend ? ld_fresh(sel + i) : -1;
     }
   };
   load_sel(wbeg);
@@ -280,7 +289,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
       const int i = i0 + u * 32 + lane;
       const bool ok = t[u] >= 0 && t[u] < ctx;
       s[u] = ok ? __ldcg(t2s + t[u]) : -1;
-      r[u] = (ok && res) ? __ldcg(res + t[u]) : -1;
+      r[u] = (ok && res) ? ld_fresh(res + t[u]) : -1;
       if (i < wend) {
         s_sel[i] = t[u];
         if (t[u] >= ctx) bad |= HS_DEVERR_RANGE;
@@ -592,7 +601,7 @@ __global__ void hs_gather_kernel(const uint8_t* __restrict__ base, int64_t req_s
       if (c < n) {
         const int r = (int)(c / cpr);
         const int w = (int)(c - (long long)r * cpr);
-        const int t = __ldcg(idx + r);
+        const int t = ld_fresh(idx + r);
         if (t >= 0 && t < limit) {
           const uint8_t* p = base + (size_t)(r / k) * (size_t)req_stride + (size_t)t * row_bytes + ((size_t)w << 4);
           v[u] = FROM_HOST ? load_row_chunk_host(p) : __ldcg(reinterpret_cast<const uint4*>(p));

@@ -35,6 +35,15 @@
  * programmatic dependent launch: each waits for the preceding kernel in its stream before touching memory.
  * Pointers, batch and k are baked into a captured graph; refill topk_idx in place between replays.
  * The hs_get_* readers synchronise the device. No function is thread-safe on the same pool.
+ *
+ * Where the per-call arrays may live: topk_idx, resident_row and out_slots may be device memory or page-locked
+ * host memory mapped into the device's address space (hs_host_alloc, or cudaHostAlloc with
+ * cudaHostAllocMapped; pass the device-side address, which equals the host address under unified addressing,
+ * as on GB300). The kernels then read the selection and write the slots over the host link (NVLink-C2C)
+ * themselves, with no separate copy; index loads always fetch afresh, so the host may rewrite a selection
+ * buffer between calls. Host-side writes must be complete before the call is enqueued, and out_slots in host
+ * memory may be read once the stream has been synchronised. Metadata, hot buffer and pool stay as described
+ * in hs_pool_desc.
  */
 #ifndef HS_H_
 #define HS_H_
@@ -134,8 +143,8 @@ int hs_step_begin(hs_pool *pool, hs_stream_t stream);
 /*
  * Resolve one layer's selections for requests 0..batch-1 (batch row b is pool request b) at the current step:
  * hit test, LRU victim choice, metadata update and the fetch of every missing row into its hot slot, in one
- * kernel ("HiSparse" paper, Abstract). topk_idx: device int32 [batch][k], row-major; out_slots: device int32
- * [batch][k], written in input order. 1 <= batch <= max_batch, 1 <= k <= topk_max; batch == 0 or k == 0 is a
+ * kernel ("HiSparse" paper, Abstract). topk_idx: int32 [batch][k], row-major; out_slots: int32 [batch][k],
+ * written in input order (device or mapped host memory, see above). 1 <= batch <= max_batch, 1 <= k <= topk_max; batch == 0 or k == 0 is a
  * no-op. Enqueued on `stream`.
  */
 int hs_resolve(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk_idx, int32_t k,
@@ -165,11 +174,12 @@ int hs_resolve_shared(hs_pool *pool, int32_t layer0, int32_t nlayers, int32_t ba
 
 /*
  * Three-tier variant ("Hybrid HiSparse" knowledge card, Timeline: resident, hot and missing rows resolved in one
- * fused pass; hot pages come from ordinary KV blocks of the same memory pool). resident_row: device int32, for
- * request b at resident_row + b*resident_stride (resident_stride >= ctx), the row of each token still held in
- * the ordinary HBM KV pool (0 <= row <= 2^31 - 3), or -1. A selected token that is not in the hot buffer but is
- * resident there is served in place: it takes no slot, refreshes no stamp, is fetched from nowhere, counts as a
- * hit, and its out_slot is -2 - row. A hot-buffer hit takes precedence. Everything else is as hs_resolve.
+ * fused pass; hot pages come from ordinary KV blocks of the same memory pool). resident_row: int32, for request
+ * b at resident_row + b*resident_stride (resident_stride >= ctx; normally device memory), the row of each token
+ * still held in the ordinary HBM KV pool (0 <= row <= 2^31 - 3), or -1. A selected token that is not in the hot
+ * buffer but is resident there is served in place: it takes no slot, refreshes no stamp, is fetched from nowhere,
+ * counts as a hit, and its out_slot is -2 - row. A hot-buffer hit takes precedence. Everything else is as
+ * hs_resolve.
  */
 int hs_resolve_tiered(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk_idx, int32_t k,
                       const int32_t *resident_row, int64_t resident_stride, int32_t *out_slots,

@@ -233,3 +233,50 @@ def test_resolve_shared_small_and_ragged(batch):
     with pytest.raises(hs.HsError):
         hs.hs_resolve_shared(buf.handle, 3, 3, batch, t, k, outs[0])  # past the last layer
     buf.close()
+
+
+@pytest.mark.parametrize("ctx", [6000, 300000])  # token bitmap and radix miss ranking
+def test_selection_and_slots_in_mapped_host_memory(ctx):
+    """The selection is read from, and out_slots written to, page-locked mapped host memory by the kernel itself
+    (no copies). The same host buffers are rewritten every step, so a stale copy of a host line would show; the
+    results equal the device-memory path's and the oracle's. The gather reads its slot list from host memory too."""
+    rng = np.random.default_rng(ctx)
+    batch, slots, k, R = 6, 400, 96, 64
+    dev = _pool(1, batch, ctx, slots, k, R, seed=5)
+    hst = _pool(1, batch, ctx, slots, k, R, seed=5)
+    ora = oracle.OraclePool(ctx, slots, R, 1, batch, track_rows=False)
+    sel_h = hs.HostBuffer(batch * k * 4)
+    out_h = hs.HostBuffer(batch * k * 4)
+    gat_h = torch.empty((batch, k, R), dtype=torch.uint8, device="cuda")
+    gat_d = torch.empty_like(gat_h)
+    sel_np = np.frombuffer(sel_h.numpy(), dtype=np.int32).reshape(batch, k)
+    out_np = np.frombuffer(out_h.numpy(), dtype=np.int32).reshape(batch, k)
+    stream = torch.cuda.Stream()
+    prev = None
+    for step in range(12):
+        prev = _rand_sel(rng, batch, k, ctx, prev, keep=0.0 if step == 6 else 0.6, pad=0.03)
+        sel_np[:] = prev
+        out_np[:] = -9
+        t = torch.from_numpy(prev).cuda()
+        out_d = torch.full((batch, k), -9, dtype=torch.int32, device="cuda")
+        with torch.cuda.stream(stream):
+            hs.hs_step_begin(dev.handle, stream)
+            hs.hs_step_begin(hst.handle, stream)
+            hs.hs_resolve(dev.handle, 0, batch, t, k, out_d, stream)
+            hs.hs_resolve(hst.handle, 0, batch, sel_h.ptr, k, out_h.ptr, stream)
+            hs.hs_gather(dev.handle, 0, batch, out_d, k, gat_d, stream)
+            hs.hs_gather(hst.handle, 0, batch, out_h.ptr, k, gat_h, stream)
+        stream.synchronize()
+        ora.step_begin()
+        expect = ora.resolve(0, prev, None)
+        assert np.array_equal(out_d.cpu().numpy(), expect), step
+        assert np.array_equal(out_np, expect), step
+        assert torch.equal(gat_h, gat_d), step
+    for name in ("tok2slot", "slot_tok", "slot_stamp", "counters"):
+        assert torch.equal(dev.view(name), hst.view(name)), name
+    assert torch.equal(dev.hot_view(), hst.hot_view())
+    _check_rows(hst)
+    for b in (dev, hst):
+        b.close()
+    sel_h.close()
+    out_h.close()
