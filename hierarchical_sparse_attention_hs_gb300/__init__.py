@@ -21,7 +21,8 @@ __all__ = [
     "hs_pool_reset", "hs_step_begin", "hs_resolve", "hs_prefetch", "hs_get_error", "hs_get_counters",
     "hs_pool_destroy", "hs_host_alloc", "hs_host_free", "hs_error_string", "HS_DEVERR_RANGE", "HS_DEVERR_DUP",
     "HS_DEVERR_STATE", "HostBuffer", "PoolBuffers", "hs_probe_link", "hs_gather", "hs_gather_history",
-    "hs_resolve_shared", "hs_resolve_tiered",
+    "hs_resolve_shared", "hs_resolve_tiered", "hs_mla_decode", "hs_mla_decode_history", "HS_DEVERR_TIMEOUT",
+    "MLA_HEADS", "MLA_D_QK", "MLA_D_V",
 ]
 
 HS_OK = 0
@@ -33,6 +34,8 @@ HS_ERR_UNSUPPORTED = -5
 HS_DEVERR_RANGE = 1
 HS_DEVERR_DUP = 2
 HS_DEVERR_STATE = 4
+HS_DEVERR_TIMEOUT = 8
+MLA_HEADS, MLA_D_QK, MLA_D_V = 128, 576, 512  # shape of the sparse MLA decode consumer
 
 LIB_PATH = _build_mod.LIB_PATH
 _lib = None
@@ -81,6 +84,9 @@ def load():
             "hs_resolve_shared": (ctypes.c_int, [vp, i32, i32, i32, vp, i32, vp, vp]),
             "hs_resolve_tiered": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, ctypes.c_int64, vp, vp]),
             "hs_gather_history": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp]),
+            "hs_mla_decode": (ctypes.c_int, [vp, i32, i32, vp, vp, i32, vp, ctypes.c_int64, ctypes.c_float, vp, vp,
+                                             vp]),
+            "hs_mla_decode_history": (ctypes.c_int, [vp, i32, i32, vp, vp, i32, ctypes.c_float, vp, vp, vp]),
             "hs_get_error": (ctypes.c_int, [vp, P(i32), i32]),
             "hs_get_counters": (ctypes.c_int, [vp, i32, P(ctypes.c_uint64)]),
             "hs_pool_destroy": (ctypes.c_int, [vp]),
@@ -179,6 +185,18 @@ def hs_resolve_tiered(pool: int, layer: int, batch: int, topk_idx, k: int, resid
 
 def hs_gather(pool: int, layer: int, batch: int, out_slots, k: int, dst, stream=None) -> None:
     _check(load().hs_gather(pool, layer, batch, _addr(out_slots), k, _addr(dst), _stream(stream)), "hs_gather")
+
+
+def hs_mla_decode(pool: int, layer: int, batch: int, q, out_slots, k: int, resident_rows, resident_count: int,
+                  sm_scale: float, out, lse, stream=None) -> None:
+    _check(load().hs_mla_decode(pool, layer, batch, _addr(q), _addr(out_slots), k, _addr(resident_rows),
+                                resident_count, sm_scale, _addr(out), _addr(lse), _stream(stream)), "hs_mla_decode")
+
+
+def hs_mla_decode_history(pool: int, layer: int, batch: int, q, topk_idx, k: int, sm_scale: float, out, lse,
+                          stream=None) -> None:
+    _check(load().hs_mla_decode_history(pool, layer, batch, _addr(q), _addr(topk_idx), k, sm_scale, _addr(out),
+                                        _addr(lse), _stream(stream)), "hs_mla_decode_history")
 
 
 def hs_gather_history(pool: int, layer: int, batch: int, topk_idx, k: int, dst, stream=None) -> None:

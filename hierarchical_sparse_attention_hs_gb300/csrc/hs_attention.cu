@@ -1,0 +1,493 @@
+// Sparse MLA decode attention over the rows a resolve selected, sm_103a (tcgen05 tensor cores, TMEM accumulators).
+//
+// The resolver exists so that a sparse-attention kernel reads the selected KV rows from the GPU hot buffer
+// instead of the full history, with model outputs unchanged ("HiSparse" paper, Abstract; the "Hybrid HiSparse"
+// knowledge card builds on Sparse MLA). This is that consumer for one decode step of multi-head latent attention
+// in its absorbed form: each row is 576 bf16 values (the 512-dimensional latent, then the 64-dimensional rotary
+// key), 128 query heads each have a 576-dimensional query, and per request
+//
+//     s[h][i] = sm_scale * q[h] . row_i,   out[h] = sum_i softmax_i(s[h]) * row_i[0:512],   lse[h] = log sum_i e^s
+//
+// over the valid selected rows. The same kernel reads the rows either through a slot list (the hot buffer, plus
+// rows still held in the ordinary HBM pool for entries -2 - row) or by token from the full history, so the two
+// results are bit-identical whenever the rows are.
+//
+// One CTA computes all 128 heads of one request for one half of the 512 value columns (grid = 2 x batch; both
+// halves compute the scores). Warp roles:
+//   warps 0-3  softmax: thread h owns head h, which is TMEM lane h of the score and output accumulators;
+//   warp 4     lane 0 issues every tcgen05.mma (and warp 4 allocates / frees the tensor memory);
+//   warps 5-6  load key rows into shared memory with cp.async (zero rows for padding), 16 rows per block.
+// Shared memory: Q (128 x 576, 144 KB), three key stages (16 rows each) and two P buffers, all in the
+// no-swizzle interleaved layout: element (row r, column c) at (r/8)*G + (c/8)*128 + (r%8)*16 + (c%8)*2, where G
+// is the byte size of an 8-row group. The key stage serves the score GEMM as a K-major operand (rows = keys) and
+// the value GEMM as an MN-major operand (the same bytes read with the two strides exchanged).
+// Tensor memory (512 columns): two 16-column score buffers, and the 256-column output half at column 256.
+// Per key block j: S = Q K^T (36 MMAs of 128x16x16) into score buffer j%2; the softmax warps read it, update the
+// running max m (raised only when a block's maximum exceeds it by more than 8 in log2 units, which bounds P
+// and O by 2^8 and makes the rescale of O rare), write P = 2^(s - m) rounded to bf16 into P buffer j%2, and
+// sum the rounded values; then O += P V (one 128x256x16 MMA). Score block j+1 overlaps the softmax of block j.
+// mbarriers order the roles; every wait is bounded: on running out it sets an abort flag that ends every role
+// and the HS_DEVERR_TIMEOUT bit of the pool's error word, after the issued MMAs and copies have drained.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/hs.h"
+#include "hs_pool.hpp"
+
+namespace {
+
+constexpr int HEADS = 128;
+constexpr int DQK = 576;
+constexpr int DV = 512;
+constexpr int DV_HALF = DV / 2;
+constexpr int ROW_BYTES = DQK * 2;
+constexpr int KB = 16;      // keys per block
+constexpr int NSTAGE = 3;   // key stages
+constexpr int CHUNKS = DQK / 8;            // 16-byte chunks per row
+constexpr int GROUP = CHUNKS * 128;        // bytes of one 8-row group of a 576-column matrix
+constexpr int Q_BYTES = HEADS * ROW_BYTES;
+constexpr int STAGE_BYTES = KB * ROW_BYTES;
+constexpr int P_GROUP = (KB / 8) * 128;    // bytes of one 8-head group of P (128 x 16)
+constexpr int P_BYTES = HEADS * KB * 2;
+constexpr int SOFTMAX_WARPS = 4, MMA_WARP = 4, LOAD_WARP0 = 5, LOAD_WARPS = 2;
+constexpr int NTHREADS = (SOFTMAX_WARPS + 1 + LOAD_WARPS) * 32;
+constexpr int LOAD_THREADS = LOAD_WARPS * 32;
+constexpr uint32_t TMEM_COLS = 512, TMEM_S = 0, TMEM_O = 256;
+constexpr unsigned WAIT_LIMIT = 1u << 20;  // try_wait rounds (each may suspend briefly) before a wait gives up
+
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int OFF_P = OFF_K + NSTAGE * STAGE_BYTES;
+constexpr int OFF_KEY = OFF_P + 2 * P_BYTES;  // row pointers of each stage: [NSTAGE][KB]
+// mbarriers: kfull[3] kempty[3] sfull[2] sempty[2] pfull[2] pdone[2] odone drain
+constexpr int NBAR = 16;
+constexpr int OFF_BAR = OFF_KEY + NSTAGE * KB * 8;
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM address, abort flag
+constexpr int SMEM_BYTES = OFF_MISC + 16;
+
+struct MlaArgs {
+  const uint16_t* q;        // bf16 [batch][HEADS][DQK]
+  const int32_t* idx;       // [batch][k]: slots (mode 0) or tokens (mode 1)
+  int32_t k;
+  int32_t mode;             // 0: slot list into `rows` (+ resident rows); 1: tokens into `rows`
+  const uint8_t* rows;      // request 0's rows of this layer
+  int64_t req_stride;       // bytes between requests in `rows`
+  int32_t limit;            // valid indices into `rows` are 0 .. limit-1
+  const uint8_t* resident;  // mode 0: rows for entries -2 - r, or nullptr
+  int64_t resident_count;
+  float scale_log2;         // sm_scale * log2(e)
+  float* out;               // [batch][HEADS][DV]
+  float* lse;               // [batch][HEADS]
+  int32_t* err;
+};
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ int32_t ld_fresh(const int32_t* p) {
+  int32_t v;
+  asm("ld.global.cv.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(su32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// shared-memory writes of this thread become visible to the tensor cores' (async proxy) reads
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void bar_init(uint64_t* b, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool bar_test(uint64_t* b, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of the given parity; false once the abort flag is set or after WAIT_LIMIT rounds (which
+// sets it).
+__device__ __forceinline__ bool bar_wait(uint64_t* b, unsigned parity, volatile int* abort_flag) {
+  for (unsigned it = 0; it < WAIT_LIMIT; ++it) {
+    if (bar_test(b, parity)) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, no swizzle: start, leading-dimension and stride-dimension byte offsets.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+// Instruction descriptor: bf16 x bf16 -> f32, M x N, operand majors (0 = K-major, 1 = MN-major).
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* b) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b))
+               : "memory");
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane (the warp reads its 32-lane quarter together)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// Address of the row an index names, or nullptr for padding / out-of-range entries (masked keys).
+__device__ __forceinline__ const uint8_t* row_of(const MlaArgs& a, int b, int32_t e) {
+  if (e >= 0) return e < a.limit ? a.rows + (size_t)b * (size_t)a.req_stride + (size_t)e * ROW_BYTES : nullptr;
+  if (a.mode == 0 && e <= -2 && a.resident) {
+    const long long r = -2LL - (long long)e;
+    return r < a.resident_count ? a.resident + (size_t)r * ROW_BYTES : nullptr;
+  }
+  return nullptr;
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x >> 1, half = blockIdx.x & 1;
+  const int k = a.k, nb = (k + KB - 1) / KB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t *kfull = bars, *kempty = bars + 3, *sfull = bars + 6, *sempty = bars + 8, *pfull = bars + 10,
+           *pdone = bars + 12, *odone = bars + 14, *drain = bars + 15;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  const uint8_t** keyp = reinterpret_cast<const uint8_t**>(smem + OFF_KEY);
+
+  // Q into shared memory: head h, columns 8c..8c+7 at (h/8)*GROUP + c*128 + (h%8)*16
+  const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q + (size_t)b * HEADS * DQK);
+  for (int e = tid; e < HEADS * CHUNKS; e += NTHREADS) {
+    const int h = e / CHUNKS, c = e - h * CHUNKS;
+    cp_async16(smem + OFF_Q + (h >> 3) * GROUP + c * 128 + (h & 7) * 16, qsrc + (size_t)h * ROW_BYTES + c * 16);
+  }
+  cp_async_commit();
+  if (tid == 0) {
+    for (int i = 0; i < NSTAGE; ++i) {
+      bar_init(kfull + i, LOAD_THREADS);
+      bar_init(kempty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      bar_init(sfull + i, 1);
+      bar_init(sempty + i, SOFTMAX_WARPS * 32);
+      bar_init(pfull + i, SOFTMAX_WARPS * 32);
+      bar_init(pdone + i, 1);
+    }
+    bar_init(odone, 1);
+    bar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == MMA_WARP) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tslot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  cp_async_wait_all();
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp >= LOAD_WARP0) {
+    // ---- loaders: block j into stage j % NSTAGE once the value GEMM of block j - NSTAGE has read it
+    const int lt = tid - LOAD_WARP0 * 32;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      const int s = j % NSTAGE;
+      if (ok && j >= NSTAGE) ok = bar_wait(kempty + s, (unsigned)((j / NSTAGE) - 1) & 1u, abort_flag);
+      if (ok && lt < KB) {
+        const int i = j * KB + lt;
+        keyp[s * KB + lt] = i < k ? row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i)) : nullptr;
+      }
+      named_sync(1, LOAD_THREADS);  // every loader thread reaches it in every block, aborted or not
+      if (ok) {
+        uint8_t* st = smem + OFF_K + s * STAGE_BYTES;
+        for (int e = lt; e < KB * CHUNKS; e += LOAD_THREADS) {
+          const int i = e / CHUNKS, c = e - i * CHUNKS;
+          uint8_t* dst = st + (i >> 3) * GROUP + c * 128 + (i & 7) * 16;
+          const uint8_t* src = keyp[s * KB + i];
+          if (src)
+            cp_async16(dst, src + c * 16);
+          else
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      cp_async_commit();
+      if (ok && j >= 1) {  // block j - 1 has landed
+        cp_async_wait_one_pending();
+        fence_proxy_async();
+        bar_arrive(kfull + (j - 1) % NSTAGE);
+      }
+    }
+    cp_async_wait_all();
+    fence_proxy_async();
+    if (ok && nb > 0) bar_arrive(kfull + (nb - 1) % NSTAGE);
+  } else if (warp == MMA_WARP) {
+    // ---- one thread issues the tensor-core work: scores of block j, then the value GEMM of block j - 1
+    if (lane == 0) {
+      const uint32_t q0 = su32(smem + OFF_Q), k0 = su32(smem + OFF_K), p0 = su32(smem + OFF_P);
+      constexpr uint32_t ID_QK = idesc_bf16(128, KB, 0, 0);
+      constexpr uint32_t ID_PV = idesc_bf16(128, DV_HALF, 0, 1);
+      bool ok = true;
+      for (int j = 0; j <= nb && ok; ++j) {
+        if (j < nb) {
+          const int s = j % NSTAGE, sb = j & 1;
+          ok = bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag);
+          if (ok && j >= 2) ok = bar_wait(sempty + sb, (unsigned)((j - 2) >> 1) & 1u, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kb = k0 + s * STAGE_BYTES;
+#pragma unroll 4
+          for (int kk = 0; kk < DQK / 16; ++kk)
+            mma_bf16(tmem + TMEM_S + sb * KB, sdesc(q0 + kk * 256, 128, GROUP), sdesc(kb + kk * 256, 128, GROUP),
+                     ID_QK, kk > 0);
+          mma_commit(sfull + sb);
+        }
+        if (j >= 1) {
+          const int jp = j - 1, s = jp % NSTAGE, pb = jp & 1;
+          ok = bar_wait(pfull + pb, (unsigned)(jp >> 1) & 1u, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          // P (K-major: keys are K) times the value half of the key rows (MN-major: the value columns are N)
+          mma_bf16(tmem + TMEM_O, sdesc(p0 + pb * P_BYTES, 128, P_GROUP),
+                   sdesc(k0 + s * STAGE_BYTES + half * (DV_HALF / 8) * 128, GROUP, 128), ID_PV, jp > 0);
+          mma_commit(kempty + s);
+          mma_commit(pdone + pb);
+          if (jp == nb - 1) mma_commit(odone);
+        }
+      }
+      // every issued MMA has finished before the tensor memory is freed
+      mma_commit(drain);
+      for (unsigned it = 0; it < WAIT_LIMIT && !bar_test(drain, 0); ++it) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- softmax: thread h = head h = TMEM lane h
+    const int h = tid;
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      const int s = j % NSTAGE, sb = j & 1;
+      ok = __all_sync(0xffffffffu, ok && bar_wait(sfull + sb, (unsigned)(j >> 1) & 1u, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      float sv[16];
+      tmem_ld16(trow + TMEM_S + sb * KB, sv);
+      tc_fence_before();
+      bar_arrive(sempty + sb);
+      // the stage's row pointers (written by the loaders before they signalled the stage full)
+      ok = __all_sync(0xffffffffu, bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag));
+      if (!ok) break;
+      const uint8_t* const* kp = keyp + s * KB;
+      float x[16];
+      float mb = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        x[i] = kp[i] ? sv[i] * a.scale_log2 : -INFINITY;
+        mb = fmaxf(mb, x[i]);
+      }
+      float m_new = m_run;
+      if (mb > -INFINITY && (m_run == -INFINITY || mb > m_run + 8.f)) m_new = mb;
+      const bool resc = m_new != m_run && m_run != -INFINITY;
+      if (__any_sync(0xffffffffu, resc)) {
+        // O holds blocks 0 .. j-1 once the value GEMM of block j-1 has finished; scale this warp's rows
+        ok = __all_sync(0xffffffffu, bar_wait(pdone + ((j - 1) & 1), (unsigned)((j - 1) >> 1) & 1u, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const float f = resc ? exp2f(m_run - m_new) : 1.f;
+        for (int c = 0; c < DV_HALF; c += 16) {
+          float o[16];
+          tmem_ld16(trow + TMEM_O + c, o);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] *= f;
+          tmem_st16(trow + TMEM_O + c, o);
+        }
+        tmem_wait_st();
+        l_run *= f;
+      }
+      m_run = m_new;
+      uint32_t pk[8];
+      float psum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const __nv_bfloat16 lo = __float2bfloat16_rn(x[2 * i] == -INFINITY ? 0.f : exp2f(x[2 * i] - m_run));
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x[2 * i + 1] == -INFINITY ? 0.f : exp2f(x[2 * i + 1] - m_run));
+        psum += __bfloat162float(lo) + __bfloat162float(hi);
+        pk[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+      }
+      l_run += psum;
+      // P buffer sb is free once the value GEMM of block j-2 has read it
+      if (j >= 2) {
+        ok = __all_sync(0xffffffffu, bar_wait(pdone + sb, (unsigned)((j - 2) >> 1) & 1u, abort_flag));
+        if (!ok) break;
+      }
+      uint8_t* prow = smem + OFF_P + sb * P_BYTES + (h >> 3) * P_GROUP + (h & 7) * 16;
+      *reinterpret_cast<uint4*>(prow) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4*>(prow + 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      fence_proxy_async();
+      tc_fence_before();
+      bar_arrive(pfull + sb);
+    }
+    if (ok && nb > 0) ok = __all_sync(0xffffffffu, bar_wait(odone, 0, abort_flag));
+    if (ok) {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      float* orow = a.out + ((size_t)b * HEADS + h) * DV + half * DV_HALF;
+      for (int c = 0; c < DV_HALF; c += 16) {
+        float o[16];
+        if (nb > 0) {
+          tmem_ld16(trow + TMEM_O + c, o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(orow + c + i) = make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+      }
+      if (half == 0)
+        a.lse[(size_t)b * HEADS + h] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+  if (tid == 0 && *abort_flag) atomicOr(a.err, HS_DEVERR_TIMEOUT);
+}
+
+int launch_mla(hs_pool* p, int32_t batch, const MlaArgs& a, cudaStream_t s) {
+  if (cudaFuncSetAttribute(hs_mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_UNSUPPORTED;
+  }
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)(2 * batch), 1, 1);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  (void)p;
+  return cudaLaunchKernelEx(&cfg, hs_mla_decode_kernel, a) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+bool common_args_ok(const hs_pool* p, int32_t layer, int32_t batch, const void* q, const int32_t* idx, int32_t k,
+                    const float* out, const float* lse) {
+  if (!p || layer < 0 || layer >= p->d.layers || batch < 0 || batch > p->d.max_batch || k < 0) return false;
+  if (batch == 0 || k == 0) return true;
+  return q && idx && out && lse && !(reinterpret_cast<uintptr_t>(q) & 15) && !(reinterpret_cast<uintptr_t>(out) & 15);
+}
+
+}  // namespace
+
+extern "C" int hs_mla_decode(hs_pool* pool, int32_t layer, int32_t batch, const void* q, const int32_t* out_slots,
+                             int32_t k, const void* resident_rows, int64_t resident_count, float sm_scale, float* out,
+                             float* lse, hs_stream_t stream) {
+  if (!common_args_ok(pool, layer, batch, q, out_slots, k, out, lse) || resident_count < 0 ||
+      (resident_rows && (reinterpret_cast<uintptr_t>(resident_rows) & 15)))
+    return HS_ERR_INVALID_ARG;
+  if (pool->d.row_bytes != ROW_BYTES) return HS_ERR_UNSUPPORTED;
+  if (batch == 0 || k == 0) return HS_OK;
+  const size_t hrl = (size_t)pool->d.slots * ROW_BYTES;
+  MlaArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = static_cast<const uint16_t*>(q);
+  a.idx = out_slots;
+  a.k = k;
+  a.mode = 0;
+  a.rows = static_cast<const uint8_t*>(pool->d.hot_buf) + (size_t)layer * (size_t)pool->d.max_batch * hrl;
+  a.req_stride = (int64_t)hrl;
+  a.limit = pool->d.slots;
+  a.resident = static_cast<const uint8_t*>(resident_rows);
+  a.resident_count = resident_rows ? resident_count : 0;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.out = out;
+  a.lse = lse;
+  a.err = pool->err;
+  return launch_mla(pool, batch, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int hs_mla_decode_history(hs_pool* pool, int32_t layer, int32_t batch, const void* q,
+                                     const int32_t* topk_idx, int32_t k, float sm_scale, float* out, float* lse,
+                                     hs_stream_t stream) {
+  if (!common_args_ok(pool, layer, batch, q, topk_idx, k, out, lse)) return HS_ERR_INVALID_ARG;
+  if (pool->d.row_bytes != ROW_BYTES) return HS_ERR_UNSUPPORTED;
+  if (batch == 0 || k == 0) return HS_OK;
+  MlaArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = static_cast<const uint16_t*>(q);
+  a.idx = topk_idx;
+  a.k = k;
+  a.mode = 1;
+  a.rows = pool->src + (size_t)layer * (size_t)pool->d.host_layer_stride;
+  a.req_stride = pool->d.host_req_stride ? pool->d.host_req_stride : (int64_t)pool->d.ctx * ROW_BYTES;
+  a.limit = pool->d.ctx;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.out = out;
+  a.lse = lse;
+  a.err = pool->err;
+  return launch_mla(pool, batch, a, reinterpret_cast<cudaStream_t>(stream));
+}

@@ -14,8 +14,8 @@
 // There is no spin-wait anywhere.
 //
 // Per CTA (512 threads), in shared memory:
-//   1. load the selection row, slot stamps and slot tokens; clear the hit bitmap (and the token bitmap); each
-//      warp keeps the min and max stamp it saw;
+//   1. the slot stamps and slot tokens start for shared memory as asynchronous copies while each warp loads its
+//      run of the selection row; clear the hit bitmap (and the token bitmap);
 //   2. each warp gathers tok2slot for its run of selection entries (random 4-byte reads, several in flight per
 //      thread); a hit sets its slot's bit in the hit bitmap, a miss its token's bit in the token bitmap (a bit
 //      found set already is a repeated token);
@@ -26,8 +26,8 @@
 //         count over the token bitmap (contexts up to 2^18 units; longer ones radix-sort the misses by token);
 //      B (warps 8-15): the victims -- a stable LSD radix sort (8-bit digits, per-warp digit rows, ranks from
 //         ballots, so the order is exact and deterministic) of the slots not hit, keyed by stamp - min stamp
-//         (one pass while the stamps span fewer than 256 steps); the first m are the victims in (stamp, slot)
-//         order;
+//         (one pass while the stamps span fewer than 256 steps; the stamp range is read from shared memory);
+//         the first m are the victims in (stamp, slot) order;
 //   5. group A, after the cluster barrier, per owned selection entry: a hit is stamped; a miss of rank j takes
 //      victim j (the old token is unmapped, the new one mapped, the slot stamped); out_slots in input order;
 //   6. rows: the row chunks are split between the cluster's CTAs in interleaved runs of blocks of
@@ -47,6 +47,7 @@
 
 #include "../../include/hs.h"
 #include "hs_block.cuh"
+#include "hs_pool.hpp"
 
 namespace {
 
@@ -58,7 +59,7 @@ using hs::RED_INTS;
 using hs::TBL_STRIDE;
 
 constexpr int COPY_UNROLL = 8;  // 16-byte loads in flight per thread in the copy loops
-constexpr int MAX_CLUSTER = 8;
+constexpr int MAX_CLUSTER = HS_MAX_CLUSTER;
 constexpr int GA_WARPS = NW / 2;                 // group A: miss ranks and the first wave of row loads
 constexpr int GA_THREADS = GA_WARPS * 32;
 constexpr int BITMAP_MAX_CTX = 1 << 18;          // longer contexts rank misses with the radix sort
@@ -648,24 +649,6 @@ __global__ void hs_probe_read_kernel(const uint8_t* __restrict__ src, size_t n16
 // --------------------------------------------------------------------------------------------------------------
 // Host side
 // --------------------------------------------------------------------------------------------------------------
-struct hs_pool {
-  hs_pool_desc d;
-  hs_meta_layout lay;
-  int device;
-  int num_sms;
-  bool noio;
-  const uint8_t* src;  // device-visible row source
-  int32_t* step;
-  int32_t* err;
-  unsigned long long* counters;
-  int32_t* tok2slot;
-  int32_t* slot_tok;
-  int32_t* slot_stamp;
-  size_t smem;
-  int max_cluster;   // largest cluster size that fits on the device for this shared-memory size
-  int resident;      // resolve CTAs resident on the device at once (one wave)
-  int max_active[MAX_CLUSTER + 1];  // clusters of each size resident at once
-};
 
 namespace {
 

@@ -72,6 +72,7 @@ typedef struct hs_pool hs_pool;
 #define HS_DEVERR_RANGE 1 /* a selected token was >= ctx */
 #define HS_DEVERR_DUP 2   /* a token appeared twice in one selection row */
 #define HS_DEVERR_STATE 4 /* metadata found inconsistent (never set by correct use) */
+#define HS_DEVERR_TIMEOUT 8 /* a kernel's bounded wait ran out and it stopped early (never set by correct use) */
 
 /*
  * Geometry and memory of a pool of layers x max_batch request-layers.
@@ -198,6 +199,32 @@ int hs_gather(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *out_sl
  * source when the pool has one; a zero row for an index < 0 or >= ctx). */
 int hs_gather_history(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk_idx, int32_t k, void *dst,
                       hs_stream_t stream);
+
+/*
+ * Consumer: sparse MLA decode attention over the rows a resolve selected, on the tensor cores (the read that the
+ * hot buffer exists for: "HiSparse" paper, Abstract, model outputs unchanged; the "Hybrid HiSparse" knowledge card
+ * builds on Sparse MLA). Absorbed multi-head latent attention, one decode step: every row is 576 bf16 values (the
+ * 512-value latent, then the 64-value rotary key), so the pool's row_bytes must be 1152 (else
+ * HS_ERR_UNSUPPORTED). For request b < batch and head h < 128, over the valid entries i of its slot list:
+ *     s[h][i] = sm_scale * dot(q[b][h][0:576], row_i),
+ *     out[b][h][0:512] = sum_i softmax_i(s[h]) * row_i[0:512],   lse[b][h] = ln sum_i exp(s[h][i]).
+ * out_slots [batch][k] as a resolve wrote it (device or mapped host memory): an entry >= 0 names hot slot
+ * `entry` of `layer`; an entry <= -2 names row -2 - entry of resident_rows (device, 1152-byte rows, count rows;
+ * NULL for none), as hs_resolve_tiered writes them; -1 and anything else is padding. q: device bf16
+ * [batch][128][576], 16-byte aligned; out: device fp32 [batch][128][512], 16-byte aligned; lse: device fp32
+ * [batch][128]. With no valid entry a head's output is zero and its lse -inf. P is rounded to bf16 before the
+ * value product and the normaliser sums the rounded weights; scores and outputs accumulate in fp32. Enqueued on
+ * `stream`; batch == 0 or k == 0 is a no-op.
+ */
+int hs_mla_decode(hs_pool *pool, int32_t layer, int32_t batch, const void *q, const int32_t *out_slots, int32_t k,
+                  const void *resident_rows, int64_t resident_count, float sm_scale, float *out, float *lse,
+                  hs_stream_t stream);
+
+/* The same attention read from the full history, for comparison: entry i of topk_idx names token i of request
+ * b's rows in the pool's row source (the no-IO copy when the pool has one, else the host pool); indices < 0 or
+ * >= ctx are padding. Equal rows in the same order give bit-identical out and lse. */
+int hs_mla_decode_history(hs_pool *pool, int32_t layer, int32_t batch, const void *q, const int32_t *topk_idx,
+                          int32_t k, float sm_scale, float *out, float *lse, hs_stream_t stream);
 
 /* Synchronise the device, then read the sticky device error word into *out (HS_DEVERR_* bits); clear it when
  * `clear` is non-zero. */

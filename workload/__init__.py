@@ -112,6 +112,9 @@ WORKLOADS = {
                       steps=128, keep_pct=75, dist=UNIFORM),
     "shared": Workload("shared", 5, layers=78, requests=8, ctx=1048576, topk=2048, slots=8192, row_bytes=656,
                        steps=32, keep_pct=85, dist=ZIPF, zipf_s=1.05, shared_across_layers=True),
+    # the dsa stream with rows an attention kernel can read: 576 bf16 values (512 latent + 64 rotary)
+    "mla": Workload("mla", 6, layers=1, requests=32, ctx=131072, topk=2048, slots=4096, row_bytes=1152, steps=32,
+                    keep_pct=80, dist=ZIPF, zipf_s=1.1, row_kind=ROWS_BF16_NORMAL),
 }
 
 
@@ -216,3 +219,11 @@ def gen_resident(ctx: int, batch: int, steps: int, seed: int, window: int = 256,
             rows = (blocks[:, None] * page + np.arange(page)[None, :]).astype(np.int32)
             out[s, b].reshape(npages, page)[pages] = rows
     return out
+
+
+def gen_queries(batch: int, heads: int, dim: int, seed: int) -> np.ndarray:
+    """Decode queries as bf16 bit patterns uint16 [batch][heads][dim]: N(0,1) float32 draws (numpy generator
+    seeded by (seed, batch, heads, dim)) rounded to nearest even."""
+    rng = np.random.default_rng([seed, 0x9E37, batch, heads, dim])
+    f = rng.standard_normal((batch, heads, dim), dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((f + 0x7FFF + ((f >> 16) & 1)) >> 16).astype(np.uint16)
