@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -43,6 +44,7 @@ import workload as wl  # noqa: E402
 METRIC = "top-k selections resolved/s"
 UNIT = "selections/s"
 FLUSH_BYTES = 256 << 20
+MLA_SCALE = 1.0 / math.sqrt(192.0)  # softmax scale of the attention consumer: 1/sqrt(128 + 64)
 
 
 def describe(w: wl.Workload) -> str:
@@ -162,7 +164,8 @@ class GpuRun:
 
     def __init__(self, w: wl.Workload, noio: bool = False, prefetch: bool = False, host: object = None,
                  host_layers: int | None = None, layer_work_mb: float = 0.0, work_only: bool = False,
-                 full_offload: bool = False, shared_call: bool = False, tiered_frac: float | None = None):
+                 full_offload: bool = False, shared_call: bool = False, tiered_frac: float | None = None,
+                 attention: bool = False):
         import torch
 
         import hierarchical_sparse_attention_hs_gb300 as hs
@@ -197,6 +200,14 @@ class GpuRun:
         self.shared_call = shared_call and w.shared_across_layers
         # Three-tier resolution: per step, a resident map of the tokens still held in the HBM KV pool (one map per
         # request, shared by all layers as a block table is), kept in device memory like the pool's block table
+        # Sparse MLA decode after each layer's resolve, reading the rows through out_slots (576 bf16 per row)
+        self.attention = attention
+        if attention:
+            if w.row_bytes != hs.MLA_D_QK * 2:
+                raise ValueError("--attention needs 1152-byte rows (the mla workload)")
+            self.q = torch.from_numpy(wl.gen_queries(w.requests, hs.MLA_HEADS, hs.MLA_D_QK, w.seed).view(np.int16)).cuda()
+            self.att_out = torch.empty((w.requests, hs.MLA_HEADS, hs.MLA_D_V), dtype=torch.float32, device="cuda")
+            self.att_lse = torch.empty((w.requests, hs.MLA_HEADS), dtype=torch.float32, device="cuda")
         self.res = None
         if tiered_frac is not None:
             self.res = torch.from_numpy(wl.gen_resident(w.ctx, w.requests, w.steps, w.seed, frac=tiered_frac)).cuda()
@@ -245,7 +256,14 @@ class GpuRun:
         self.hs.hs_step_begin(self.pool, self.stream)
         self.enqueue_resolves(s)
 
+    def enqueue_attention(self, l):
+        w = self.w
+        self.hs.hs_mla_decode(self.pool, l, w.requests, self.q, self._out(l), w.topk, None, 0, MLA_SCALE,
+                              self.att_out, self.att_lse, self.stream)
+
     def enqueue_layer_work(self, l):
+        if self.attention:
+            self.enqueue_attention(l)
         if not self.layer_work:
             return
         w = self.w
@@ -303,6 +321,8 @@ class GpuRun:
         return g
 
     def launches_per_step(self) -> int:
+        if self.attention:
+            return 1 + 2 * self.w.layers
         if self.work_only or self.full_offload:
             return self.w.layers
         if self.shared_call:
@@ -405,6 +425,31 @@ class GpuRun:
         host_sel.close()
         host_out.close()
         return ms, self.sel[0].numel() * 4, self.out.numel() * 4, match
+
+    def attention_pass(self, k_steps: int) -> dict:
+        """The attention consumer alone, on the slot lists the last step left: one graph per layer's launch
+        replayed k_steps times, L2 flushed before each, CUDA events around each launch on its stream."""
+        torch, w = self.torch, self.w
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            self.enqueue_attention(0)
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(k_steps):
+            self.flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(self.stream):
+                e0.record(self.stream)
+                g.replay()
+                e1.record(self.stream)
+            times.append((e0, e1))
+        self.stream.synchronize()
+        ms = [a.elapsed_time(b) for a, b in times]
+        slots = self.out[0].cpu().numpy()
+        valid = int(((slots >= 0) & (slots < w.slots)).sum())
+        flops = 2.0 * self.hs.MLA_HEADS * valid * (self.hs.MLA_D_QK + self.hs.MLA_D_V)
+        return {"ms": statistics.mean(ms), "ms_p50": float(np.percentile(ms, 50)), "valid_rows": valid,
+                "flops": flops}
 
     def e2e_copy_pass(self, k_steps: int):
         """The same loop with explicit copies: per step, copy the selections in from pinned host memory, run the
@@ -600,7 +645,8 @@ def run_gpu(args) -> int:
     w = wl.WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
     run = GpuRun(w, prefetch=args.prefetch, layer_work_mb=args.layer_work_mb, work_only=args.work_only,
-                 full_offload=args.full_offload, shared_call=args.shared_call, tiered_frac=args.tiered_frac)
+                 full_offload=args.full_offload, shared_call=args.shared_call, tiered_frac=args.tiered_frac,
+                 attention=args.attention)
     # The GPU reads the whole host pool once (as a long-running server has long since done), so that first-touch
     # address translation of host pages is not charged to the timed steps; it also measures the link.
     link_zc, link_cp = measure_link(hs, torch, run.buf.host.ptr, run.buf.host.nbytes // 16 * 16)
@@ -662,6 +708,24 @@ def run_gpu(args) -> int:
                        f"HBM {hbm_peak:.1f} GB/s {hbm_src}",
     }
 
+    attention = None
+    if args.attention:
+        # the consumer alone, on the slot lists of the sequence's last step (steady state)
+        a = run.attention_pass(K)
+        bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+        tflops = a["flops"] / (a["ms"] / 1e3) / 1e12
+        attention = {
+            "kernel": "hs_mla_decode_kernel", "bound": "tensor", "achieved": tflops, "peak": bf16_peak,
+            "unit": "TFLOP/s", "frac": tflops / bf16_peak, "ms_per_launch": a["ms"], "ms_per_launch_p50": a["ms_p50"],
+            "flops_per_launch": a["flops"], "valid_rows_per_launch": a["valid_rows"],
+            "flops_definition": "2 * 128 heads * valid rows * (576 + 512): the score and value products that "
+                                "are needed (the kernel also recomputes the scores in its second value half)",
+            "row_bytes_per_launch": 2 * a["valid_rows"] * w.row_bytes,
+            "peak_source": "bf16_tflops (cuBLAS bf16 GEMM, burst) in MEASURED_PEAKS.json" if "bf16_tflops" in peaks
+                           else "fallback 1900 TFLOP/s",
+            "timing": "CUDA events around one graph launch each, L2 flushed before each, on the launch stream",
+        }
+
     # end to end through the public API with host buffers: zero-copy (the kernels read the selections from and
     # write out_slots to mapped host memory), and with explicit staging copies
     e2e_ms, h2d, d2h, e2e_match = run.e2e_pass(K)
@@ -715,7 +779,7 @@ def run_gpu(args) -> int:
                    "graphs": "one CUDA graph per decode step", "prefetch": bool(args.prefetch),
                    "layer_work_mb": args.layer_work_mb, "work_only": bool(args.work_only),
                    "full_offload": bool(args.full_offload), "shared_call": bool(args.shared_call),
-                   "tiered_frac": args.tiered_frac},
+                   "tiered_frac": args.tiered_frac, "attention": bool(args.attention)},
         "selected_entries_per_s": value * w.topk,
         "miss_gbs": miss_bytes / (total_ms / 1e3) / 1e9 * world,
         "cold_step_ms": statistics.mean(cold) if cold else None,
@@ -725,6 +789,7 @@ def run_gpu(args) -> int:
         "noio": noio,
         "e2e": e2e,
         "gpu_launches": K * run.launches_per_step(),
+        "attention": attention,
         "clocks": clocks,
     }
     if rank == 0 and not args.skip_cpu:
@@ -763,10 +828,16 @@ def main() -> int:
     ap.add_argument("--tiered-frac", type=float, default=None,
                     help="three-tier resolution: fraction of pages still held in the HBM KV pool (plus the newest "
                          "256 tokens), one resident map per request and step")
+    ap.add_argument("--attention", action="store_true",
+                    help="sparse MLA decode (hs_mla_decode) after each layer's resolve; needs 1152-byte rows (the "
+                         "mla workload); adds the attention kernel's tensor-core roofline")
     ap.add_argument("--ref-layers", type=int, default=1, help="reference arm: layers resolved per step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.attention and (args.tiered_frac is not None or args.full_offload or args.work_only):
+        ap.error("--attention reads the slot lists of plain resolves; it combines with none of --tiered-frac, "
+                 "--full-offload, --work-only")
     if args.tiered_frac is not None and (args.prefetch or args.shared_call or args.full_offload):
         ap.error("--tiered-frac resolves each layer with its own call; it combines with none of --prefetch, "
                  "--shared-call, --full-offload")

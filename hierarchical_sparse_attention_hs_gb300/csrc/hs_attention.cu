@@ -16,16 +16,18 @@
 // halves compute the scores). Warp roles:
 //   warps 0-3  softmax: thread h owns head h, which is TMEM lane h of the score and output accumulators;
 //   warp 4     lane 0 issues every tcgen05.mma (and warp 4 allocates / frees the tensor memory);
-//   warps 5-6  load key rows into shared memory with cp.async (zero rows for padding), 16 rows per block.
-// Shared memory: Q (128 x 576, 144 KB), three key stages (16 rows each) and two P buffers, all in the
+//   warps 5-12 load key rows into shared memory with cp.async (zero rows for padding), 32 rows per block; four
+//              warps own each key stage and signal each block as soon as their copies have landed.
+// Shared memory: Q (128 x 576, 144 KB), two key stages (32 rows each) and one P buffer, all in the
 // no-swizzle interleaved layout: element (row r, column c) at (r/8)*G + (c/8)*128 + (r%8)*16 + (c%8)*2, where G
 // is the byte size of an 8-row group. The key stage serves the score GEMM as a K-major operand (rows = keys) and
 // the value GEMM as an MN-major operand (the same bytes read with the two strides exchanged).
-// Tensor memory (512 columns): two 16-column score buffers, and the 256-column output half at column 256.
-// Per key block j: S = Q K^T (36 MMAs of 128x16x16) into score buffer j%2; the softmax warps read it, update the
+// Tensor memory (512 columns): two 32-column score buffers, and the 256-column output half at column 256.
+// Per key block j: S = Q K^T (36 MMAs of 128x32x16) into score buffer j%2; the softmax warps read it, update the
 // running max m (raised only when a block's maximum exceeds it by more than 8 in log2 units, which bounds P
-// and O by 2^8 and makes the rescale of O rare), write P = 2^(s - m) rounded to bf16 into P buffer j%2, and
-// sum the rounded values; then O += P V (one 128x256x16 MMA). Score block j+1 overlaps the softmax of block j.
+// and O by 2^8 and makes the rescale of O rare), write P = 2^(s - m) rounded to bf16 into the P buffer once
+// the value GEMM of block j-1 has read it, and sum the rounded values; then O += P V (two 128x256x16 MMAs).
+// The score GEMM of block j+1 overlaps the softmax of block j.
 // mbarriers order the roles; every wait is bounded: on running out it sets an abort flag that ends every role
 // and the HS_DEVERR_TIMEOUT bit of the pool's error word, after the issued MMAs and copies have drained.
 
@@ -45,29 +47,33 @@ constexpr int DQK = 576;
 constexpr int DV = 512;
 constexpr int DV_HALF = DV / 2;
 constexpr int ROW_BYTES = DQK * 2;
-constexpr int KB = 16;      // keys per block
-constexpr int NSTAGE = 3;   // key stages
+constexpr int KB = 32;     // keys per block (the N of the score GEMM)
+constexpr int NSTAGE = 2;  // key stages, one loader warp each
+constexpr int NPB = 1;     // P buffers
 constexpr int CHUNKS = DQK / 8;            // 16-byte chunks per row
 constexpr int GROUP = CHUNKS * 128;        // bytes of one 8-row group of a 576-column matrix
 constexpr int Q_BYTES = HEADS * ROW_BYTES;
 constexpr int STAGE_BYTES = KB * ROW_BYTES;
 constexpr int P_GROUP = (KB / 8) * 128;    // bytes of one 8-head group of P (128 x 16)
 constexpr int P_BYTES = HEADS * KB * 2;
-constexpr int SOFTMAX_WARPS = 4, MMA_WARP = 4, LOAD_WARP0 = 5, LOAD_WARPS = 2;
+constexpr int SOFTMAX_WARPS = 4, MMA_WARP = 4, LOAD_WARP0 = 5;
+constexpr int STAGE_WARPS = 4;                  // loader warps per key stage
+constexpr int LOAD_WARPS = NSTAGE * STAGE_WARPS;
 constexpr int NTHREADS = (SOFTMAX_WARPS + 1 + LOAD_WARPS) * 32;
-constexpr int LOAD_THREADS = LOAD_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512, TMEM_S = 0, TMEM_O = 256;
 constexpr unsigned WAIT_LIMIT = 1u << 20;  // try_wait rounds (each may suspend briefly) before a wait gives up
 
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + Q_BYTES;
 constexpr int OFF_P = OFF_K + NSTAGE * STAGE_BYTES;
-constexpr int OFF_KEY = OFF_P + 2 * P_BYTES;  // row pointers of each stage: [NSTAGE][KB]
-// mbarriers: kfull[3] kempty[3] sfull[2] sempty[2] pfull[2] pdone[2] odone drain
-constexpr int NBAR = 16;
+constexpr int OFF_KEY = OFF_P + NPB * P_BYTES;  // row pointers of each stage: [NSTAGE][KB]
+// mbarriers: kfull[NSTAGE] kempty[NSTAGE] sfull[2] sempty[2] pfull[NPB] pdone[NPB] odone drain
+constexpr int NBAR = 2 * NSTAGE + 4 + 2 * NPB + 2;
 constexpr int OFF_BAR = OFF_KEY + NSTAGE * KB * 8;
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM address, abort flag
-constexpr int SMEM_BYTES = OFF_MISC + 16;
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM address, abort flag, per-stage stop flags
+constexpr int SMEM_BYTES = OFF_MISC + 8 + 4 * NSTAGE;
+static_assert(SMEM_BYTES <= 232448, "shared memory per block");
+static_assert(KB == 32, "one loader lane per key of a block");
 
 struct MlaArgs {
   const uint16_t* q;        // bf16 [batch][HEADS][DQK]
@@ -98,7 +104,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_one_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// fetch a row into L2 ahead of its copy (bytes: multiple of 16)
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 // shared-memory writes of this thread become visible to the tensor cores' (async proxy) reads
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -176,9 +185,8 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
       "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
       : "memory");
 }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Address of the row an index names, or nullptr for padding / out-of-range entries (masked keys).
 __device__ __forceinline__ const uint8_t* row_of(const MlaArgs& a, int b, int32_t e) {
@@ -198,10 +206,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   const int b = blockIdx.x >> 1, half = blockIdx.x & 1;
   const int k = a.k, nb = (k + KB - 1) / KB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t *kfull = bars, *kempty = bars + 3, *sfull = bars + 6, *sempty = bars + 8, *pfull = bars + 10,
-           *pdone = bars + 12, *odone = bars + 14, *drain = bars + 15;
+  uint64_t *kfull = bars, *kempty = bars + NSTAGE, *sfull = bars + 2 * NSTAGE, *sempty = sfull + 2,
+           *pfull = sempty + 2, *pdone = pfull + NPB, *odone = pdone + NPB, *drain = odone + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  volatile int* stage_stop = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
   const uint8_t** keyp = reinterpret_cast<const uint8_t**>(smem + OFF_KEY);
 
   // Q into shared memory: head h, columns 8c..8c+7 at (h/8)*GROUP + c*128 + (h%8)*16
@@ -213,18 +222,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   cp_async_commit();
   if (tid == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
-      bar_init(kfull + i, LOAD_THREADS);
+      bar_init(kfull + i, STAGE_WARPS * 32);
       bar_init(kempty + i, 1);
     }
     for (int i = 0; i < 2; ++i) {
       bar_init(sfull + i, 1);
       bar_init(sempty + i, SOFTMAX_WARPS * 32);
+    }
+    for (int i = 0; i < NPB; ++i) {
       bar_init(pfull + i, SOFTMAX_WARPS * 32);
       bar_init(pdone + i, 1);
     }
     bar_init(odone, 1);
     bar_init(drain, 1);
     *abort_flag = 0;
+    for (int i = 0; i < NSTAGE; ++i) stage_stop[i] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == MMA_WARP) {
@@ -241,47 +253,77 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   const uint32_t tmem = *tslot;
 
   if (warp >= LOAD_WARP0) {
-    // ---- loaders: block j into stage j % NSTAGE once the value GEMM of block j - NSTAGE has read it
-    const int lt = tid - LOAD_WARP0 * 32;
-    bool ok = true;
-    for (int j = 0; j < nb; ++j) {
-      const int s = j % NSTAGE;
-      if (ok && j >= NSTAGE) ok = bar_wait(kempty + s, (unsigned)((j / NSTAGE) - 1) & 1u, abort_flag);
-      if (ok && lt < KB) {
-        const int i = j * KB + lt;
-        keyp[s * KB + lt] = i < k ? row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i)) : nullptr;
-      }
-      named_sync(1, LOAD_THREADS);  // every loader thread reaches it in every block, aborted or not
-      if (ok) {
-        uint8_t* st = smem + OFF_K + s * STAGE_BYTES;
-        for (int e = lt; e < KB * CHUNKS; e += LOAD_THREADS) {
-          const int i = e / CHUNKS, c = e - i * CHUNKS;
-          uint8_t* dst = st + (i >> 3) * GROUP + c * 128 + (i & 7) * 16;
-          const uint8_t* src = keyp[s * KB + i];
-          if (src)
-            cp_async16(dst, src + c * 16);
-          else
-            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    // ---- loaders: the STAGE_WARPS warps of stage s fill it with blocks s, s + NSTAGE, ...: the stage's first
+    //      warp waits until the value GEMM of the block NSTAGE earlier has read the stage and looks up the 32 rows
+    //      (lane i: key i), a named barrier releases the others, every thread copies its share of the 16-byte
+    //      chunks, and each signals the stage full as its copies land. The stop decision is read after the
+    //      barrier, so the stage's threads leave the loop together.
+    const int ws = warp - LOAD_WARP0, s = ws / STAGE_WARPS, sub = ws % STAGE_WARPS;
+    uint8_t* st = smem + OFF_K + s * STAGE_BYTES;
+    for (int j = s; j < nb; j += NSTAGE) {
+      if (sub == 0) {
+        bool ok = j < NSTAGE ||
+                  __all_sync(0xffffffffu, bar_wait(kempty + s, (unsigned)((j / NSTAGE) - 1) & 1u, abort_flag));
+        if (ok) {
+          const int i = j * KB + lane;
+          keyp[s * KB + lane] = i < k ? row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i)) : nullptr;
+        } else if (lane == 0) {
+          stage_stop[s] = 1;
         }
       }
-      cp_async_commit();
-      if (ok && j >= 1) {  // block j - 1 has landed
-        cp_async_wait_one_pending();
-        fence_proxy_async();
-        bar_arrive(kfull + (j - 1) % NSTAGE);
+      named_sync(1 + s, STAGE_WARPS * 32);
+      if (stage_stop[s]) break;
+      for (int e = sub * 32 + lane; e < KB * CHUNKS; e += STAGE_WARPS * 32) {
+        const int r = e / CHUNKS, c = e - r * CHUNKS;
+        uint8_t* dst = st + (r >> 3) * GROUP + c * 128 + (r & 7) * 16;
+        const uint8_t* src = keyp[s * KB + r];
+        if (src)
+          cp_async16(dst, src + c * 16);
+        else
+          *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
       }
+      cp_async_commit();
+      if (sub == 0) {
+        // the rows of this stage's next block start for L2 while these copies land, so that its copies read
+        // L2 rather than DRAM
+        const int i2 = (j + NSTAGE) * KB + lane;
+        if (i2 < k) {
+          const uint8_t* r2 = row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i2));
+          if (r2) prefetch_l2(r2, ROW_BYTES);
+        }
+      }
+      cp_async_wait_all();
+      fence_proxy_async();
+      bar_arrive(kfull + s);
     }
     cp_async_wait_all();
-    fence_proxy_async();
-    if (ok && nb > 0) bar_arrive(kfull + (nb - 1) % NSTAGE);
   } else if (warp == MMA_WARP) {
-    // ---- one thread issues the tensor-core work: scores of block j, then the value GEMM of block j - 1
+    // ---- one thread issues the tensor-core work: scores of block j, and the value GEMM of block j - 1
     if (lane == 0) {
       const uint32_t q0 = su32(smem + OFF_Q), k0 = su32(smem + OFF_K), p0 = su32(smem + OFF_P);
       constexpr uint32_t ID_QK = idesc_bf16(128, KB, 0, 0);
       constexpr uint32_t ID_PV = idesc_bf16(128, DV_HALF, 0, 1);
       bool ok = true;
+      // The value GEMM of block j-1 goes in as soon as its P is ready: pfull is polled between quarters of the
+      // score GEMM of block j (the tensor pipe runs in issue order), so the key stage of block j-1 is released
+      // without waiting for all of block j's scores.
+      auto issue_pv = [&](int jp) {
+        const int s = jp % NSTAGE, pb = jp % NPB;
+        tc_fence_after();
+        // P (K-major: keys are K) times the value half of the key rows (MN-major: the value columns are N),
+        // 16 keys (two 8-key groups) per MMA
+        const uint32_t vb = k0 + s * STAGE_BYTES + half * (DV_HALF / 8) * 128;
+#pragma unroll
+        for (int kk = 0; kk < KB / 16; ++kk)
+          mma_bf16(tmem + TMEM_O, sdesc(p0 + pb * P_BYTES + kk * 256, 128, P_GROUP),
+                   sdesc(vb + kk * 2 * GROUP, GROUP, 128), ID_PV, (jp > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(kempty + s);
+        mma_commit(pdone + pb);
+        if (jp == nb - 1) mma_commit(odone);
+      };
       for (int j = 0; j <= nb && ok; ++j) {
+        bool pv_pending = j >= 1;
+        const int jp = j - 1;
         if (j < nb) {
           const int s = j % NSTAGE, sb = j & 1;
           ok = bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag);
@@ -289,23 +331,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
           if (!ok) break;
           tc_fence_after();
           const uint32_t kb = k0 + s * STAGE_BYTES;
-#pragma unroll 4
-          for (int kk = 0; kk < DQK / 16; ++kk)
-            mma_bf16(tmem + TMEM_S + sb * KB, sdesc(q0 + kk * 256, 128, GROUP), sdesc(kb + kk * 256, 128, GROUP),
-                     ID_QK, kk > 0);
+          constexpr int NK = DQK / 16, QUARTER = NK / 4;
+#pragma unroll 1
+          for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+            for (int kq = 0; kq < QUARTER; ++kq) {
+              const int kk = q4 * QUARTER + kq;
+              mma_bf16(tmem + TMEM_S + sb * KB, sdesc(q0 + kk * 256, 128, GROUP), sdesc(kb + kk * 256, 128, GROUP),
+                       ID_QK, kk > 0);
+            }
+            if (pv_pending && bar_test(pfull + jp % NPB, (unsigned)(jp / NPB) & 1u)) {
+              issue_pv(jp);
+              pv_pending = false;
+            }
+          }
           mma_commit(sfull + sb);
         }
-        if (j >= 1) {
-          const int jp = j - 1, s = jp % NSTAGE, pb = jp & 1;
-          ok = bar_wait(pfull + pb, (unsigned)(jp >> 1) & 1u, abort_flag);
+        if (pv_pending) {
+          ok = bar_wait(pfull + jp % NPB, (unsigned)(jp / NPB) & 1u, abort_flag);
           if (!ok) break;
-          tc_fence_after();
-          // P (K-major: keys are K) times the value half of the key rows (MN-major: the value columns are N)
-          mma_bf16(tmem + TMEM_O, sdesc(p0 + pb * P_BYTES, 128, P_GROUP),
-                   sdesc(k0 + s * STAGE_BYTES + half * (DV_HALF / 8) * 128, GROUP, 128), ID_PV, jp > 0);
-          mma_commit(kempty + s);
-          mma_commit(pdone + pb);
-          if (jp == nb - 1) mma_commit(odone);
+          issue_pv(jp);
         }
       }
       // every issued MMA has finished before the tensor memory is freed
@@ -325,18 +370,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       ok = __all_sync(0xffffffffu, ok && bar_wait(sfull + sb, (unsigned)(j >> 1) & 1u, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      float sv[16];
-      tmem_ld16(trow + TMEM_S + sb * KB, sv);
+      float sv[KB];
+#pragma unroll
+      for (int c = 0; c < KB; c += 16) tmem_ld16(trow + TMEM_S + sb * KB + c, *reinterpret_cast<float(*)[16]>(sv + c));
       tc_fence_before();
       bar_arrive(sempty + sb);
       // the stage's row pointers (written by the loaders before they signalled the stage full)
       ok = __all_sync(0xffffffffu, bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag));
       if (!ok) break;
       const uint8_t* const* kp = keyp + s * KB;
-      float x[16];
+      float x[KB];
       float mb = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < KB; ++i) {
         x[i] = kp[i] ? sv[i] * a.scale_log2 : -INFINITY;
         mb = fmaxf(mb, x[i]);
       }
@@ -345,7 +391,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       const bool resc = m_new != m_run && m_run != -INFINITY;
       if (__any_sync(0xffffffffu, resc)) {
         // O holds blocks 0 .. j-1 once the value GEMM of block j-1 has finished; scale this warp's rows
-        ok = __all_sync(0xffffffffu, bar_wait(pdone + ((j - 1) & 1), (unsigned)((j - 1) >> 1) & 1u, abort_flag));
+        ok = __all_sync(0xffffffffu,
+                        bar_wait(pdone + ((j - 1) % NPB), (unsigned)((j - 1) / NPB) & 1u, abort_flag));
         if (!ok) break;
         tc_fence_after();
         const float f = resc ? exp2f(m_run - m_new) : 1.f;
@@ -360,27 +407,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
         l_run *= f;
       }
       m_run = m_new;
-      uint32_t pk[8];
+      uint32_t pk[KB / 2];
       float psum = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < KB / 2; ++i) {
         const __nv_bfloat16 lo = __float2bfloat16_rn(x[2 * i] == -INFINITY ? 0.f : exp2f(x[2 * i] - m_run));
         const __nv_bfloat16 hi = __float2bfloat16_rn(x[2 * i + 1] == -INFINITY ? 0.f : exp2f(x[2 * i + 1] - m_run));
         psum += __bfloat162float(lo) + __bfloat162float(hi);
         pk[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
       }
       l_run += psum;
-      // P buffer sb is free once the value GEMM of block j-2 has read it
-      if (j >= 2) {
-        ok = __all_sync(0xffffffffu, bar_wait(pdone + sb, (unsigned)((j - 2) >> 1) & 1u, abort_flag));
+      // P buffer pb is free once the value GEMM of block j - NPB has read it
+      const int pb = j % NPB;
+      if (j >= NPB) {
+        ok = __all_sync(0xffffffffu, bar_wait(pdone + pb, (unsigned)((j - NPB) / NPB) & 1u, abort_flag));
         if (!ok) break;
       }
-      uint8_t* prow = smem + OFF_P + sb * P_BYTES + (h >> 3) * P_GROUP + (h & 7) * 16;
-      *reinterpret_cast<uint4*>(prow) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<uint4*>(prow + 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      uint8_t* prow = smem + OFF_P + pb * P_BYTES + (h >> 3) * P_GROUP + (h & 7) * 16;
+#pragma unroll
+      for (int c = 0; c < KB / 8; ++c)
+        *reinterpret_cast<uint4*>(prow + c * 128) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async();
       tc_fence_before();
-      bar_arrive(pfull + sb);
+      bar_arrive(pfull + pb);
     }
     if (ok && nb > 0) ok = __all_sync(0xffffffffu, bar_wait(odone, 0, abort_flag));
     if (ok) {
