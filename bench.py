@@ -128,12 +128,15 @@ class ClockSampler:
 
 
 def kernel_sources_sha16() -> str:
+    """Hash of the files the resolve kernel is compiled from (its translation unit and the headers it includes),
+    which a committed ncu capture of that kernel must match."""
     import hashlib
 
     from hierarchical_sparse_attention_hs_gb300 import build as hs_build
 
-    parts = [hashlib.sha256(open(f, "rb").read()).hexdigest() for f in
-             [p for p in hs_build.SOURCES] + [hs_build.HEADERS[1]]]
+    csrc = os.path.join(os.path.dirname(hs_build.__file__), "csrc")
+    files = [os.path.join(csrc, n) for n in ("hs_resolve.cu", "hs_block.cuh", "hs_pool.hpp")]
+    parts = [hashlib.sha256(open(f, "rb").read()).hexdigest() for f in files]
     return hashlib.sha256("".join(parts).encode()).hexdigest()[:16]
 
 
