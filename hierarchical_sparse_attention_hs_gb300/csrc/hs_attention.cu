@@ -12,24 +12,34 @@
 // rows still held in the ordinary HBM pool for entries -2 - row) or by token from the full history, so the two
 // results are bit-identical whenever the rows are.
 //
-// One CTA computes all 128 heads of one request for one half of the 512 value columns (grid = 2 x batch; both
-// halves compute the scores). Warp roles:
-//   warps 0-3  softmax: thread h owns head h, which is TMEM lane h of the score and output accumulators;
-//   warp 4     lane 0 issues every tcgen05.mma (and warp 4 allocates / frees the tensor memory);
-//   warps 5-12 load key rows into shared memory with cp.async (zero rows for padding), 32 rows per block; four
-//              warps own each key stage and signal each block as soon as their copies have landed.
-// Shared memory: Q (128 x 576, 144 KB), two key stages (32 rows each) and one P buffer, all in the
-// no-swizzle interleaved layout: element (row r, column c) at (r/8)*G + (c/8)*128 + (r%8)*16 + (c%8)*2, where G
-// is the byte size of an 8-row group. The key stage serves the score GEMM as a K-major operand (rows = keys) and
-// the value GEMM as an MN-major operand (the same bytes read with the two strides exchanged).
+// The two CTAs of a request form a thread-block cluster and split the score GEMM's 576 columns: CTA 0 holds
+// columns 0..255 of Q and of every selected row, CTA 1 columns 256..575. Each computes partial scores over its
+// columns on the tensor cores, sends them to the other through distributed shared memory, and adds the other's.
+// Both then hold the same S (addition commutes), run the same softmax, and each multiplies P by its own value
+// half (columns 0..255 or 256..511, which lie within its columns). Half of Q per CTA leaves room for four key
+// stages, and no score work is repeated.
+// Warp roles per CTA:
+//   warps 0-3   softmax: thread h owns head h, which is TMEM lane h of the score and output accumulators;
+//   warp 4      lane 0 issues every tcgen05.mma (and warp 4 allocates / frees the tensor memory);
+//   warps 5-12  load the CTA's columns of the selected rows into shared memory with cp.async (zero rows for
+//               padding), 32 rows per block, two warps per key stage, prefetching each stage's next rows into L2;
+//   warp 13     hands the score-exchange buffers back to the peer once they have been read.
+// Shared memory: this CTA's columns of Q (128 x 256 or 320), four key stages (32 rows each), one P buffer and two
+// exchange buffers, in the no-swizzle interleaved layout: element (row r, column c) at (r/8)*G + (c/8)*128 +
+// (r%8)*16 + (c%8)*2, where G is the byte size of an 8-row group (one spare 128-byte slot included). A key stage
+// serves the score GEMM as a K-major operand (rows = keys) and the value GEMM as an MN-major operand (the same
+// bytes read with the two strides exchanged).
 // Tensor memory (512 columns): two 32-column score buffers, and the 256-column output half at column 256.
-// Per key block j: S = Q K^T (36 MMAs of 128x32x16) into score buffer j%2; the softmax warps read it, update the
-// running max m (raised only when a block's maximum exceeds it by more than 8 in log2 units, which bounds P
-// and O by 2^8 and makes the rescale of O rare), write P = 2^(s - m) rounded to bf16 into the P buffer once
-// the value GEMM of block j-1 has read it, and sum the rounded values; then O += P V (two 128x256x16 MMAs).
-// The score GEMM of block j+1 overlaps the softmax of block j.
-// mbarriers order the roles; every wait is bounded: on running out it sets an abort flag that ends every role
-// and the HS_DEVERR_TIMEOUT bit of the pool's error word, after the issued MMAs and copies have drained.
+// Per key block j: partial S = Q K^T (16 or 20 MMAs of 128x32x16) into score buffer j%2; the softmax threads
+// read it, store it into the peer's exchange buffer with st.async (completing the bytes the peer's barrier
+// expects), wait for the peer's part, and update the running max m (raised only when a block's maximum exceeds
+// it by more than 8 in log2 units, which bounds P and O by 2^8 and makes the rescale of O rare); they write
+// P = 2^(s - m) rounded to bf16 into the P buffer once the value GEMM of block j-1 has read it, and sum the
+// rounded values; then O += P V (two 128x256x16 MMAs). The score GEMM of block j+1 overlaps the softmax of
+// block j. mbarriers order the roles, within the CTA and across the pair; every wait is bounded: on running out
+// it sets an abort flag that ends every role and the HS_DEVERR_TIMEOUT bit of the pool's error word, after the
+// issued MMAs and copies have drained. Cluster barriers at the start and the end keep each CTA's shared memory
+// alive while the other may still reach it.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -48,27 +58,36 @@ constexpr int DV = 512;
 constexpr int DV_HALF = DV / 2;
 constexpr int ROW_BYTES = DQK * 2;
 constexpr int KB = 32;     // keys per block (the N of the score GEMM)
-constexpr int NSTAGE = 2;  // key stages, one loader warp each
+constexpr int NSTAGE = 4;  // key stages
 constexpr int NPB = 1;     // P buffers
-constexpr int CHUNKS = DQK / 8;            // 16-byte chunks per row
-constexpr int GROUP = CHUNKS * 128;        // bytes of one 8-row group of a 576-column matrix
-constexpr int Q_BYTES = HEADS * ROW_BYTES;
-constexpr int STAGE_BYTES = KB * ROW_BYTES;
-constexpr int P_GROUP = (KB / 8) * 128;    // bytes of one 8-head group of P (128 x 16)
+// Score-GEMM columns of each CTA of a request's pair: CTA 0 the first DSPLIT (its value half), CTA 1 the rest,
+// which contain its value half (columns 256..511).
+constexpr int DSPLIT = 256;
+constexpr int MAX_NDIM = DQK - DSPLIT;
+// An 8-row group of a CTA's columns holds its 16-byte chunks at 128-byte spacing plus one spare 128-byte slot, so
+// that successive groups do not start at power-of-two distances.
+constexpr int MAX_GROUP = (MAX_NDIM / 8 + 1) * 128;
+constexpr int Q_BYTES = (HEADS / 8) * MAX_GROUP;
+constexpr int STAGE_BYTES = (KB / 8) * MAX_GROUP;
+constexpr int P_GROUP = (KB / 8) * 128;    // bytes of one 8-head group of P (128 x KB)
 constexpr int P_BYTES = HEADS * KB * 2;
+constexpr int X_BYTES = HEADS * KB * 4;    // the peer's partial scores of one block, fp32
 constexpr int SOFTMAX_WARPS = 4, MMA_WARP = 4, LOAD_WARP0 = 5;
-constexpr int STAGE_WARPS = 4;                  // loader warps per key stage
+constexpr int STAGE_WARPS = 2;             // loader warps per key stage
 constexpr int LOAD_WARPS = NSTAGE * STAGE_WARPS;
-constexpr int NTHREADS = (SOFTMAX_WARPS + 1 + LOAD_WARPS) * 32;
+constexpr int XCHG_WARP = LOAD_WARP0 + LOAD_WARPS;  // hands exchange buffers back to the peer
+constexpr int NTHREADS = (XCHG_WARP + 1) * 32;
 constexpr uint32_t TMEM_COLS = 512, TMEM_S = 0, TMEM_O = 256;
 constexpr unsigned WAIT_LIMIT = 1u << 20;  // try_wait rounds (each may suspend briefly) before a wait gives up
 
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + Q_BYTES;
 constexpr int OFF_P = OFF_K + NSTAGE * STAGE_BYTES;
-constexpr int OFF_KEY = OFF_P + NPB * P_BYTES;  // row pointers of each stage: [NSTAGE][KB]
-// mbarriers: kfull[NSTAGE] kempty[NSTAGE] sfull[2] sempty[2] pfull[NPB] pdone[NPB] odone drain
-constexpr int NBAR = 2 * NSTAGE + 4 + 2 * NPB + 2;
+constexpr int OFF_X = OFF_P + NPB * P_BYTES;       // two exchange buffers
+constexpr int OFF_KEY = OFF_X + 2 * X_BYTES;       // row pointers of each stage: [NSTAGE][KB]
+// mbarriers: kfull[NSTAGE] kempty[NSTAGE] sfull[2] sempty[2] pfull[NPB] pdone[NPB] odone drain xfull[2] xempty[2]
+// xread[2]
+constexpr int NBAR = 2 * NSTAGE + 4 + 2 * NPB + 2 + 6;
 constexpr int OFF_BAR = OFF_KEY + NSTAGE * KB * 8;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM address, abort flag, per-stage stop flags
 constexpr int SMEM_BYTES = OFF_MISC + 8 + 4 * NSTAGE;
@@ -126,6 +145,16 @@ __device__ __forceinline__ bool bar_test(uint64_t* b, unsigned parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of the phase of the given parity.
+__device__ __forceinline__ bool bar_poll(uint64_t* b, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase of the given parity; false once the abort flag is set or after WAIT_LIMIT rounds (which
 // sets it).
 __device__ __forceinline__ bool bar_wait(uint64_t* b, unsigned parity, volatile int* abort_flag) {
@@ -135,6 +164,51 @@ __device__ __forceinline__ bool bar_wait(uint64_t* b, unsigned parity, volatile 
   }
   *abort_flag = 1;
   return false;
+}
+
+// The pair's peer CTA: its copy of a shared-memory address, remote stores and remote arrivals.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(su32(p)), "r"(rank));
+  return r;
+}
+// asynchronous remote store; its 16 bytes count toward the transaction bytes the peer's barrier expects
+__device__ __forceinline__ void st_peer_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(mbar)
+               : "memory");
+}
+// arrive on a local barrier and expect `bytes` transaction bytes in its current phase
+__device__ __forceinline__ void bar_arrive_expect(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+// 2^x by the hardware approximation (relative error far below the bf16 rounding that follows)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void bar_arrive_peer(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+// a wait whose arrivals come from the peer (cluster-scope acquire makes its stores visible)
+__device__ __forceinline__ bool bar_wait_cluster(uint64_t* b, unsigned parity, volatile int* abort_flag) {
+  for (unsigned it = 0; it < WAIT_LIMIT; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -203,21 +277,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.x >> 1, half = blockIdx.x & 1;
+  const int b = blockIdx.x >> 1, half = blockIdx.x & 1;  // half = rank in the request's cluster of two
+  const uint32_t peer = (uint32_t)(half ^ 1);
   const int k = a.k, nb = (k + KB - 1) / KB;
+  // this CTA's score-GEMM columns: [d0, d0 + 8 * nch)
+  const int d0 = half ? DSPLIT : 0, nch = (half ? DQK - DSPLIT : DSPLIT) / 8, grp = (nch + 1) * 128;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t *kfull = bars, *kempty = bars + NSTAGE, *sfull = bars + 2 * NSTAGE, *sempty = sfull + 2,
-           *pfull = sempty + 2, *pdone = pfull + NPB, *odone = pdone + NPB, *drain = odone + 1;
+           *pfull = sempty + 2, *pdone = pfull + NPB, *odone = pdone + NPB, *drain = odone + 1, *xfull = drain + 1,
+           *xempty = xfull + 2, *xread = xempty + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   volatile int* stage_stop = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
   const uint8_t** keyp = reinterpret_cast<const uint8_t**>(smem + OFF_KEY);
 
-  // Q into shared memory: head h, columns 8c..8c+7 at (h/8)*GROUP + c*128 + (h%8)*16
-  const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q + (size_t)b * HEADS * DQK);
-  for (int e = tid; e < HEADS * CHUNKS; e += NTHREADS) {
-    const int h = e / CHUNKS, c = e - h * CHUNKS;
-    cp_async16(smem + OFF_Q + (h >> 3) * GROUP + c * 128 + (h & 7) * 16, qsrc + (size_t)h * ROW_BYTES + c * 16);
+  // this CTA's columns of Q: head h, columns d0 + 8c .. d0 + 8c + 7 at (h/8)*grp + c*128 + (h%8)*16; thread
+  // order walks that layout (8 heads of one chunk, then the next chunk), so a warp's copies fill consecutive
+  // 16-byte slots of shared memory
+  const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q + (size_t)b * HEADS * DQK) + d0 * 2;
+  for (int e = tid; e < HEADS * nch; e += NTHREADS) {
+    const int g = e / (8 * nch), rem = e - g * 8 * nch, c = rem >> 3, h = g * 8 + (rem & 7);
+    cp_async16(smem + OFF_Q + g * grp + c * 128 + (h & 7) * 16, qsrc + (size_t)h * ROW_BYTES + c * 16);
   }
   cp_async_commit();
   if (tid == 0) {
@@ -228,6 +308,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     for (int i = 0; i < 2; ++i) {
       bar_init(sfull + i, 1);
       bar_init(sempty + i, SOFTMAX_WARPS * 32);
+      bar_init(xfull + i, 1);  // one local arrival with the byte count; the peer's async stores complete it
+      bar_init(xempty + i, 1);                   // the peer's exchange warp
+      bar_init(xread + i, SOFTMAX_WARPS * 32);   // this CTA's softmax threads have read the buffer
     }
     for (int i = 0; i < NPB; ++i) {
       bar_init(pfull + i, SOFTMAX_WARPS * 32);
@@ -238,6 +321,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     *abort_flag = 0;
     for (int i = 0; i < NSTAGE; ++i) stage_stop[i] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // blocks 0 and 1 of the peer's partial scores are expected in exchange buffers 0 and 1
+    bar_arrive_expect(xfull + 0, X_BYTES);
+    bar_arrive_expect(xfull + 1, X_BYTES);
   }
   if (warp == MMA_WARP) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tslot)),
@@ -249,15 +335,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before either touches the other's shared memory
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  if (warp >= LOAD_WARP0) {
-    // ---- loaders: the STAGE_WARPS warps of stage s fill it with blocks s, s + NSTAGE, ...: the stage's first
-    //      warp waits until the value GEMM of the block NSTAGE earlier has read the stage and looks up the 32 rows
-    //      (lane i: key i), a named barrier releases the others, every thread copies its share of the 16-byte
-    //      chunks, and each signals the stage full as its copies land. The stop decision is read after the
-    //      barrier, so the stage's threads leave the loop together.
+  if (warp >= LOAD_WARP0 && warp < XCHG_WARP) {
+    // ---- loaders: the STAGE_WARPS warps of stage s fill it with blocks s, s + NSTAGE, ... (this CTA's columns
+    //      of each row): the stage's first warp waits until the value GEMM of the block NSTAGE earlier has read
+    //      the stage and looks up the 32 rows (lane i: key i), a named barrier releases the other warps, every
+    //      thread copies its share of the 16-byte chunks, and each signals the stage full as its copies land.
+    //      The stop decision is read after the barrier, so the stage's threads leave the loop together.
     const int ws = warp - LOAD_WARP0, s = ws / STAGE_WARPS, sub = ws % STAGE_WARPS;
     uint8_t* st = smem + OFF_K + s * STAGE_BYTES;
     for (int j = s; j < nb; j += NSTAGE) {
@@ -273,23 +360,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       }
       named_sync(1 + s, STAGE_WARPS * 32);
       if (stage_stop[s]) break;
-      for (int e = sub * 32 + lane; e < KB * CHUNKS; e += STAGE_WARPS * 32) {
-        const int r = e / CHUNKS, c = e - r * CHUNKS;
-        uint8_t* dst = st + (r >> 3) * GROUP + c * 128 + (r & 7) * 16;
+      // thread order walks the shared-memory layout (8 rows of one chunk, then the next chunk), so a warp's
+      // copies fill consecutive 16-byte slots
+      for (int e = sub * 32 + lane; e < KB * nch; e += STAGE_WARPS * 32) {
+        const int g = e / (8 * nch), rem = e - g * 8 * nch, c = rem >> 3, r = g * 8 + (rem & 7);
+        uint8_t* dst = st + g * grp + c * 128 + (r & 7) * 16;
         const uint8_t* src = keyp[s * KB + r];
         if (src)
-          cp_async16(dst, src + c * 16);
+          cp_async16(dst, src + d0 * 2 + c * 16);
         else
           *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
       }
       cp_async_commit();
       if (sub == 0) {
-        // the rows of this stage's next block start for L2 while these copies land, so that its copies read
-        // L2 rather than DRAM
+        // this CTA's part of the rows of the stage's next block starts for L2 while these copies land
         const int i2 = (j + NSTAGE) * KB + lane;
         if (i2 < k) {
           const uint8_t* r2 = row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i2));
-          if (r2) prefetch_l2(r2, ROW_BYTES);
+          if (r2) prefetch_l2(r2 + d0 * 2, (uint32_t)nch * 16u);
         }
       }
       cp_async_wait_all();
@@ -297,12 +385,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       bar_arrive(kfull + s);
     }
     cp_async_wait_all();
+  } else if (warp == XCHG_WARP) {
+    // ---- exchange warp: once this CTA's softmax threads have read block j from exchange buffer j % 2, it expects
+    //      block j + 2 there and lets the peer send it. Its acquire (wait) and release (remote arrive) carry the
+    //      softmax threads' reads before the peer's next stores, and keep that release off their critical path.
+    if (lane == 0) {
+      for (int j = 0; j < nb; ++j) {
+        const int xb = j & 1;
+        if (!bar_wait(xread + xb, (unsigned)(j >> 1) & 1u, abort_flag)) break;
+        if (j + 2 < nb) {
+          bar_arrive_expect(xfull + xb, X_BYTES);
+          bar_arrive_peer(peer_addr(xempty + xb, peer));
+        }
+      }
+    }
+    __syncwarp();
   } else if (warp == MMA_WARP) {
-    // ---- one thread issues the tensor-core work: scores of block j, and the value GEMM of block j - 1
+    // ---- one thread issues the tensor-core work: partial scores of block j over this CTA's columns, and the
+    //      value GEMM of block j - 1 for this CTA's value half
     if (lane == 0) {
       const uint32_t q0 = su32(smem + OFF_Q), k0 = su32(smem + OFF_K), p0 = su32(smem + OFF_P);
       constexpr uint32_t ID_QK = idesc_bf16(128, KB, 0, 0);
       constexpr uint32_t ID_PV = idesc_bf16(128, DV_HALF, 0, 1);
+      const int nk = nch / 2, quarter = nk / 4;  // MMAs of the score GEMM (16 columns each), in four parts
       bool ok = true;
       // The value GEMM of block j-1 goes in as soon as its P is ready: pfull is polled between quarters of the
       // score GEMM of block j (the tensor pipe runs in issue order), so the key stage of block j-1 is released
@@ -310,13 +415,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       auto issue_pv = [&](int jp) {
         const int s = jp % NSTAGE, pb = jp % NPB;
         tc_fence_after();
-        // P (K-major: keys are K) times the value half of the key rows (MN-major: the value columns are N),
-        // 16 keys (two 8-key groups) per MMA
-        const uint32_t vb = k0 + s * STAGE_BYTES + half * (DV_HALF / 8) * 128;
+        // P (K-major: keys are K) times this CTA's value half of the key rows, its first 256 columns (MN-major:
+        // the value columns are N), 16 keys (two 8-key groups) per MMA
+        const uint32_t vb = k0 + s * STAGE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < KB / 16; ++kk)
           mma_bf16(tmem + TMEM_O, sdesc(p0 + pb * P_BYTES + kk * 256, 128, P_GROUP),
-                   sdesc(vb + kk * 2 * GROUP, GROUP, 128), ID_PV, (jp > 0 || kk > 0) ? 1u : 0u);
+                   sdesc(vb + kk * 2 * grp, grp, 128), ID_PV, (jp > 0 || kk > 0) ? 1u : 0u);
         mma_commit(kempty + s);
         mma_commit(pdone + pb);
         if (jp == nb - 1) mma_commit(odone);
@@ -331,16 +436,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
           if (!ok) break;
           tc_fence_after();
           const uint32_t kb = k0 + s * STAGE_BYTES;
-          constexpr int NK = DQK / 16, QUARTER = NK / 4;
 #pragma unroll 1
           for (int q4 = 0; q4 < 4; ++q4) {
-#pragma unroll
-            for (int kq = 0; kq < QUARTER; ++kq) {
-              const int kk = q4 * QUARTER + kq;
-              mma_bf16(tmem + TMEM_S + sb * KB, sdesc(q0 + kk * 256, 128, GROUP), sdesc(kb + kk * 256, 128, GROUP),
-                       ID_QK, kk > 0);
+            for (int kq = 0; kq < quarter; ++kq) {
+              const int kk = q4 * quarter + kq;
+              mma_bf16(tmem + TMEM_S + sb * KB, sdesc(q0 + kk * 256, 128, grp), sdesc(kb + kk * 256, 128, grp), ID_QK,
+                       kk > 0);
             }
-            if (pv_pending && bar_test(pfull + jp % NPB, (unsigned)(jp / NPB) & 1u)) {
+            if (pv_pending && bar_poll(pfull + jp % NPB, (unsigned)(jp / NPB) & 1u)) {
               issue_pv(jp);
               pv_pending = false;
             }
@@ -360,13 +463,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     }
     __syncwarp();
   } else {
-    // ---- softmax: thread h = head h = TMEM lane h
+    // ---- softmax: thread h = head h = TMEM lane h. The partial scores of a block go to the peer, whose partial
+    //      scores come back; both CTAs then hold S = own + peer (the same value in both, addition commutes) and
+    //      run the same softmax, so their P, running max and normaliser agree bit for bit.
     const int h = tid;
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
-      const int s = j % NSTAGE, sb = j & 1;
+      const int s = j % NSTAGE, sb = j & 1, xb = j & 1;
       ok = __all_sync(0xffffffffu, ok && bar_wait(sfull + sb, (unsigned)(j >> 1) & 1u, abort_flag));
       if (!ok) break;
       tc_fence_after();
@@ -375,6 +480,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       for (int c = 0; c < KB; c += 16) tmem_ld16(trow + TMEM_S + sb * KB + c, *reinterpret_cast<float(*)[16]>(sv + c));
       tc_fence_before();
       bar_arrive(sempty + sb);
+      // the exchange buffer xb of the peer is free once the peer has read block j - 2 from it
+      if (j >= 2) {
+        ok = __all_sync(0xffffffffu, bar_wait_cluster(xempty + xb, (unsigned)((j - 2) >> 1) & 1u, abort_flag));
+        if (!ok) break;
+      }
+      // exchange buffer layout: float4 group g (scores 4g..4g+3) of head h at (g * HEADS + h) * 16; the stores
+      // complete the transaction bytes of the peer's xfull barrier, which the peer set up in advance
+      const uint8_t* xmine = smem + OFF_X + xb * X_BYTES;
+      const uint32_t xpeer = peer_addr(xmine + h * 16, peer), xfull_peer = peer_addr(xfull + xb, peer);
+#pragma unroll
+      for (int g = 0; g < KB / 4; ++g)
+        st_peer_async_v4(xpeer + g * HEADS * 16, sv[4 * g], sv[4 * g + 1], sv[4 * g + 2], sv[4 * g + 3], xfull_peer);
+      ok = __all_sync(0xffffffffu, bar_wait_cluster(xfull + xb, (unsigned)(j >> 1) & 1u, abort_flag));
+      if (!ok) break;
+#pragma unroll
+      for (int g = 0; g < KB / 4; ++g) {
+        const float4 o = *reinterpret_cast<const float4*>(xmine + (g * HEADS + h) * 16);
+        sv[4 * g] += o.x;
+        sv[4 * g + 1] += o.y;
+        sv[4 * g + 2] += o.z;
+        sv[4 * g + 3] += o.w;
+      }
+      bar_arrive(xread + xb);  // the exchange warp hands the buffer back to the peer
       // the stage's row pointers (written by the loaders before they signalled the stage full)
       ok = __all_sync(0xffffffffu, bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag));
       if (!ok) break;
@@ -395,7 +523,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
                         bar_wait(pdone + ((j - 1) % NPB), (unsigned)((j - 1) / NPB) & 1u, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        const float f = resc ? exp2f(m_run - m_new) : 1.f;
+        const float f = resc ? ex2_approx(m_run - m_new) : 1.f;
         for (int c = 0; c < DV_HALF; c += 16) {
           float o[16];
           tmem_ld16(trow + TMEM_O + c, o);
@@ -411,8 +539,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       float psum = 0.f;
 #pragma unroll
       for (int i = 0; i < KB / 2; ++i) {
-        const __nv_bfloat16 lo = __float2bfloat16_rn(x[2 * i] == -INFINITY ? 0.f : exp2f(x[2 * i] - m_run));
-        const __nv_bfloat16 hi = __float2bfloat16_rn(x[2 * i + 1] == -INFINITY ? 0.f : exp2f(x[2 * i + 1] - m_run));
+        const __nv_bfloat16 lo = __float2bfloat16_rn(x[2 * i] == -INFINITY ? 0.f : ex2_approx(x[2 * i] - m_run));
+        const __nv_bfloat16 hi =
+            __float2bfloat16_rn(x[2 * i + 1] == -INFINITY ? 0.f : ex2_approx(x[2 * i + 1] - m_run));
         psum += __bfloat162float(lo) + __bfloat162float(hi);
         pk[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
       }
@@ -455,6 +584,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the peer no longer writes into this CTA's shared memory
   if (warp == MMA_WARP) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
@@ -474,11 +604,15 @@ int launch_mla(hs_pool* p, int32_t batch, const MlaArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;  // the two CTAs of a request
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   (void)p;
   return cudaLaunchKernelEx(&cfg, hs_mla_decode_kernel, a) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
