@@ -408,6 +408,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       constexpr uint32_t ID_QK = idesc_bf16(128, KB, 0, 0);
       constexpr uint32_t ID_PV = idesc_bf16(128, DV_HALF, 0, 1);
       const int nk = nch / 2, quarter = nk / 4;  // MMAs of the score GEMM (16 columns each), in four parts
+      // Descriptors are built once; an operand 256 bytes further along is the same descriptor plus 16 in its start
+      // field (shared-memory addresses stay below 256 KB, so the 14-bit field never carries), which keeps the
+      // issue loop to a few instructions per MMA.
+      const uint64_t dq = sdesc(q0, 128, grp), dk = sdesc(k0, 128, grp), dp = sdesc(p0, 128, P_GROUP),
+                     dv = sdesc(k0, grp, 128);
       bool ok = true;
       // The value GEMM of block j-1 goes in as soon as its P is ready: pfull is polled between quarters of the
       // score GEMM of block j (the tensor pipe runs in issue order), so the key stage of block j-1 is released
@@ -417,11 +422,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
         tc_fence_after();
         // P (K-major: keys are K) times this CTA's value half of the key rows, its first 256 columns (MN-major:
         // the value columns are N), 16 keys (two 8-key groups) per MMA
-        const uint32_t vb = k0 + s * STAGE_BYTES;
+        const uint64_t da = dp + (uint64_t)((pb * P_BYTES) >> 4), db = dv + (uint64_t)((s * STAGE_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < KB / 16; ++kk)
-          mma_bf16(tmem + TMEM_O, sdesc(p0 + pb * P_BYTES + kk * 256, 128, P_GROUP),
-                   sdesc(vb + kk * 2 * grp, grp, 128), ID_PV, (jp > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16(tmem + TMEM_O, da + (uint64_t)(16 * kk), db + (uint64_t)(kk * ((2 * grp) >> 4)), ID_PV,
+                   (jp > 0 || kk > 0) ? 1u : 0u);
         mma_commit(kempty + s);
         mma_commit(pdone + pb);
         if (jp == nb - 1) mma_commit(odone);
@@ -435,13 +440,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
           if (ok && j >= 2) ok = bar_wait(sempty + sb, (unsigned)((j - 2) >> 1) & 1u, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t kb = k0 + s * STAGE_BYTES;
+          const uint64_t dkb = dk + (uint64_t)((s * STAGE_BYTES) >> 4);
+          const uint32_t dst = tmem + TMEM_S + sb * KB;
+          uint64_t a_desc = dq, b_desc = dkb;
 #pragma unroll 1
           for (int q4 = 0; q4 < 4; ++q4) {
             for (int kq = 0; kq < quarter; ++kq) {
-              const int kk = q4 * quarter + kq;
-              mma_bf16(tmem + TMEM_S + sb * KB, sdesc(q0 + kk * 256, 128, grp), sdesc(kb + kk * 256, 128, grp), ID_QK,
-                       kk > 0);
+              mma_bf16(dst, a_desc, b_desc, ID_QK, (q4 | kq) != 0);
+              a_desc += 16;  // the next 16 columns: 256 bytes further along
+              b_desc += 16;
             }
             if (pv_pending && bar_poll(pfull + jp % NPB, (unsigned)(jp / NPB) & 1u)) {
               issue_pv(jp);
