@@ -605,8 +605,7 @@ int launch_mla(hs_pool* p, int32_t batch, const MlaArgs& a, cudaStream_t s) {
     cudaGetLastError();
     return HS_ERR_UNSUPPORTED;
   }
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * batch), 1, 1);
   cfg.blockDim = dim3(NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
