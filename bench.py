@@ -770,7 +770,8 @@ def run_gpu(args) -> int:
 
     clocks = clk.summary()
     cold = [r[1] for r in per_step if r[0] == 0]
-    steady = [r[1] for r in per_step if r[0] != 0]
+    churn = [r[1] for r in per_step if r[0] in w.churn]  # steps whose selection shares nothing with the last
+    steady = [r[1] for r in per_step if r[0] != 0 and r[0] not in w.churn]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -786,6 +787,7 @@ def run_gpu(args) -> int:
         "selected_entries_per_s": value * w.topk,
         "miss_gbs": miss_bytes / (total_ms / 1e3) / 1e9 * world,
         "cold_step_ms": statistics.mean(cold) if cold else None,
+        "churn_step_ms": statistics.mean(churn) if churn else None,
         "steady_step_ms": statistics.mean(steady) if steady else None,
         "steady_step_ms_p10_p50_p90": ([float(np.percentile(steady, q)) for q in (10, 50, 90)] if steady else None),
         "roofline": roofline,

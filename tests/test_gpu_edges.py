@@ -280,3 +280,20 @@ def test_selection_and_slots_in_mapped_host_memory(ctx):
         b.close()
     sel_h.close()
     out_h.close()
+
+
+def test_probe_link_measures_and_rejects():
+    """The link probe reads a mapped host buffer with SM loads and copies it with cudaMemcpyAsync; both give a
+    positive bandwidth below the device's own copy rate, and bad arguments are refused before anything runs."""
+    host = hs.HostBuffer(64 << 20)
+    dev = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    zc, cp = hs.hs_probe_link(host.ptr, dev, 64 << 20, 2)
+    assert 1.0 < zc < 5000.0 and 1.0 < cp < 5000.0, (zc, cp)
+    with pytest.raises(hs.HsError):
+        hs.hs_probe_link(host.ptr, dev, (64 << 20) - 8, 2)  # not a multiple of 16
+    with pytest.raises(hs.HsError):
+        hs.hs_probe_link(host.ptr + 8, dev, 1 << 20, 2)  # misaligned host address
+    with pytest.raises(hs.HsError):
+        hs.hs_probe_link(host.ptr, dev, 1 << 20, 0)  # no iteration
+    torch.cuda.synchronize()
+    host.close()
