@@ -182,3 +182,25 @@ def test_decode_argument_errors():
     assert e.value.code == hs.HS_ERR_UNSUPPORTED
     hs.hs_mla_decode(buf.handle, 0, 0, q, idx, 32, None, 0, SCALE, out, lse)  # batch 0: no-op
     torch.cuda.synchronize()
+
+
+def test_decode_history_from_host_memory():
+    """With no HBM copy of the history, hs_mla_decode_history reads the rows from page-locked host memory over
+    the link; after resolves that fetched them from there too, it equals the read through the hot buffer."""
+    w = _w("mla_host", 51, requests=2, ctx=4096, topk=160, slots=640, steps=3)
+    sel_all = wl.gen_selections(w)[:, 0]
+    buf = make_pool(w)  # rows come from the host pool
+    host = buf.host.numpy().reshape(w.requests, w.ctx, w.row_bytes)
+    q_bits = wl.gen_queries(w.requests, H, DQK, w.seed)
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda()
+    out_slots = torch.empty((w.requests, w.topk), dtype=torch.int32, device="cuda")
+    vstats = _value_stats(host)
+    for s in range(w.steps):
+        topk = torch.from_numpy(sel_all[s]).cuda()
+        hs.hs_step_begin(buf.handle)
+        hs.hs_resolve(buf.handle, 0, w.requests, topk, w.topk, out_slots)
+        out_a, lse_a, out_b, lse_b = _run_pair(buf, q, out_slots, topk, w.topk, SCALE)
+        assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b), s
+        ref_out, ref_lse = _oracle(w, host, q_bits, sel_all[s], SCALE)
+        _check(out_a.cpu().numpy(), lse_a.cpu().numpy(), ref_out, ref_lse, vstats, f"host step {s}")
+    assert hs.hs_get_error(buf.handle) == 0
