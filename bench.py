@@ -653,10 +653,14 @@ def run_gpu(args) -> int:
     # The GPU reads the whole host pool once (as a long-running server has long since done), so that first-touch
     # address translation of host pages is not charged to the timed steps; it also measures the link.
     link_zc, link_cp = measure_link(hs, torch, run.buf.host.ptr, run.buf.host.nbytes // 16 * 16)
+    pool_bytes = {"host": run.buf.host.nbytes, "hot_buffer": run.buf.hot.numel(), "metadata": run.buf.meta.numel()}
     # warm-up, then a cold start for the timed region
+    nvtx = torch.cuda.nvtx
+    nvtx.range_push(f"warm-up: {W} steps of {w.name}")
     run.run_steps(W, timed=False)
     run.reset()
     run.stream.synchronize()
+    nvtx.range_pop()
 
     def barrier():
         if dist:
@@ -665,7 +669,9 @@ def run_gpu(args) -> int:
 
     barrier()
     with ClockSampler(local) as clk:
+        nvtx.range_push(f"timed: {K} steps of {w.name}")
         per_step, tot = run.run_steps(K)
+        nvtx.range_pop()
         barrier()
     step_ms = [r[1] for r in per_step]
     # The resolve launches of a step run back to back in the step's graph behind hs_step_begin, their launches
@@ -731,7 +737,9 @@ def run_gpu(args) -> int:
 
     # end to end through the public API with host buffers: zero-copy (the kernels read the selections from and
     # write out_slots to mapped host memory), and with explicit staging copies
+    nvtx.range_push("end to end, zero-copy")
     e2e_ms, h2d, d2h, e2e_match = run.e2e_pass(K)
+    nvtx.range_pop()
     e2e_ms = max_over_ranks(e2e_ms, dist)
     c_ms, c_h2d, c_d2h = run.e2e_copy_pass(K)
     c_ms = max_over_ranks(c_ms, dist)
@@ -754,9 +762,11 @@ def run_gpu(args) -> int:
         nrun = GpuRun(w, noio=True, prefetch=args.prefetch, host=host, host_layers=run.host_layers,
                       layer_work_mb=args.layer_work_mb, work_only=args.work_only, full_offload=args.full_offload,
                       shared_call=args.shared_call, tiered_frac=args.tiered_frac)
+        nvtx.range_push("no-IO")
         nrun.run_steps(W, timed=False)
         nrun.reset()
         nper, _ = nrun.run_steps(K)
+        nvtx.range_pop()
         nms = max_over_ranks(sum(r[1] for r in nper), dist)
         nk_ms = sum(r[1] for r in nper)
         n_hbm = meta + 2 * miss_bytes
@@ -781,6 +791,7 @@ def run_gpu(args) -> int:
                    "host_pool": ("one pool per layer" if run.host_layers == w.layers else
                                  "layers share one host pool (host_layer_stride 0); every miss still crosses the link"),
                    "graphs": "one CUDA graph per decode step", "prefetch": bool(args.prefetch),
+                   "pool_bytes": pool_bytes,
                    "layer_work_mb": args.layer_work_mb, "work_only": bool(args.work_only),
                    "full_offload": bool(args.full_offload), "shared_call": bool(args.shared_call),
                    "tiered_frac": args.tiered_frac, "attention": bool(args.attention)},

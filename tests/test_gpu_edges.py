@@ -297,3 +297,39 @@ def test_probe_link_measures_and_rejects():
         hs.hs_probe_link(host.ptr, dev, 1 << 20, 0)  # no iteration
     torch.cuda.synchronize()
     host.close()
+
+
+def test_checkpoint_and_resume():
+    """The pool's whole state is plain device arrays (metadata and hot buffer): copied out mid-sequence and copied
+    back later, it makes the pool replay the same steps with the same outputs and state."""
+    rng = np.random.default_rng(123)
+    batch, ctx, slots, k, R = 4, 5000, 300, 80, 64
+    buf = _pool(1, batch, ctx, slots, k, R, seed=9)
+    stream = torch.cuda.Stream()
+    sels, prev = [], None
+    for step in range(8):
+        prev = _rand_sel(rng, batch, k, ctx, prev, keep=0.5)
+        sels.append(prev)
+
+    def run(steps):
+        outs = []
+        for sel in steps:
+            out = torch.empty((batch, k), dtype=torch.int32, device="cuda")
+            with torch.cuda.stream(stream):
+                hs.hs_step_begin(buf.handle, stream)
+                hs.hs_resolve(buf.handle, 0, batch, torch.from_numpy(sel).cuda(), k, out, stream)
+            stream.synchronize()
+            outs.append(out.cpu().numpy())
+        return outs
+
+    run(sels[:4])
+    snap_meta, snap_hot = buf.meta.clone(), buf.hot.clone()
+    first = run(sels[4:])
+    end_meta, end_hot = buf.meta.clone(), buf.hot.clone()
+    buf.meta.copy_(snap_meta)  # restore the checkpoint
+    buf.hot.copy_(snap_hot)
+    torch.cuda.synchronize()
+    second = run(sels[4:])
+    assert all(np.array_equal(a, b) for a, b in zip(first, second))
+    assert torch.equal(buf.meta, end_meta) and torch.equal(buf.hot, end_hot)
+    buf.close()
