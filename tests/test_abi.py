@@ -75,3 +75,27 @@ def test_error_strings(lib):
     assert hs.hs_error_string(0) == "ok"
     assert "argument" in hs.hs_error_string(-1)
     assert hs.hs_error_string(-99) == "unknown error"
+
+
+def test_plain_c_caller(lib, tmp_path):
+    """include/hs.h is plain C: a C99 program compiles against it with warnings as errors, links libhs.so, and
+    gets the same metadata layout as the binding."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "c_caller.c")
+    exe = str(tmp_path / "c_caller")
+    libdir = os.path.dirname(hs.LIB_PATH)
+    subprocess.check_call([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                           "-I", os.path.dirname(HEADER), src, "-L", libdir, "-lhs", f"-Wl,-rpath,{libdir}",
+                           "-o", exe])
+    out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    d = hs.hs_pool_desc(2, 3, 1000, 64, 32, 656, None, 0, 0, None, None, None)
+    lay = hs.hs_get_meta_layout(d)
+    assert out[0].split() == [str(hs.hs_meta_bytes(d)), str(lay["tok2slot"]), str(lay["slot_stamp"]),
+                              str(lay["total"])]
+    assert out[1] == hs.hs_error_string(hs.HS_ERR_INVALID_ARG)
+    assert out[2].split() == [str(hs.HS_ERR_INVALID_ARG), "0"]
