@@ -12,12 +12,16 @@
 // rows still held in the ordinary HBM pool for entries -2 - row) or by token from the full history, so the two
 // results are bit-identical whenever the rows are.
 //
-// The two CTAs of a request form a thread-block cluster and split the score GEMM's 576 columns: CTA 0 holds
-// columns 0..255 of Q and of every selected row, CTA 1 columns 256..575. Each computes partial scores over its
-// columns on the tensor cores, sends them to the other through distributed shared memory, and adds the other's.
-// Both then hold the same S (addition commutes), run the same softmax, and each multiplies P by its own value
-// half (columns 0..255 or 256..511, which lie within its columns). Half of Q per CTA leaves room for four key
-// stages, and no score work is repeated.
+// A pair of CTAs splits the score GEMM's 576 columns: CTA 0 of the pair holds columns 0..255 of Q and of every
+// selected row, CTA 1 columns 256..575. Each computes partial scores over its columns on the tensor cores, sends
+// them to the other through distributed shared memory, and adds the other's. Both then hold the same S (addition
+// commutes), run the same softmax, and each multiplies P by its own value half (columns 0..255 or 256..511, which
+// lie within its columns). Half of Q per CTA leaves room for four key stages, and no score work is repeated.
+// A request's keys are split in two as well (two pairs, a cluster of four CTAs) whenever every request's cluster
+// fits on the device at once: each pair runs the softmax over its half of the key blocks, the second pair writes
+// its normalised output half to `out` and its (max, normaliser) per head into the first pair's shared memory, and
+// after a cluster barrier the first pair merges the two (flash-decoding's split-K merge, inside one cluster). A
+// pair's time is a chain of dependent steps per key block, not a bandwidth, so two pairs per request halve it.
 // Warp roles per CTA:
 //   warps 0-3   softmax: thread h owns head h, which is TMEM lane h of the score and output accumulators;
 //   warp 4      lane 0 issues every tcgen05.mma (and warp 4 allocates / frees the tensor memory);
@@ -36,7 +40,8 @@
 // it by more than 8 in log2 units, which bounds P and O by 2^8 and makes the rescale of O rare); they write
 // P = 2^(s - m) rounded to bf16 into the P buffer once the value GEMM of block j-1 has read it, and sum the
 // rounded values; then O += P V (two 128x256x16 MMAs). The score GEMM of block j+1 overlaps the softmax of
-// block j. mbarriers order the roles, within the CTA and across the pair; every wait is bounded: on running out
+// block j. The output leaves through a shared tile in whole 128-byte row segments. mbarriers order the roles,
+// within the CTA and across the pair; every wait is bounded: on running out
 // it sets an abort flag that ends every role and the HS_DEVERR_TIMEOUT bit of the pool's error word, after the
 // issued MMAs and copies have drained. Cluster barriers at the start and the end keep each CTA's shared memory
 // alive while the other may still reach it.
@@ -44,6 +49,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -90,8 +96,11 @@ constexpr int OFF_KEY = OFF_X + 2 * X_BYTES;       // row pointers of each stage
 constexpr int NBAR = 2 * NSTAGE + 4 + 2 * NPB + 2 + 6;
 constexpr int OFF_BAR = OFF_KEY + NSTAGE * KB * 8;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM address, abort flag, per-stage stop flags
-constexpr int SMEM_BYTES = OFF_MISC + 8 + 4 * NSTAGE;
+// (m, l) of every head from the CTA that ran the second key half, when a request's keys are split
+constexpr int OFF_COMB = (OFF_MISC + 8 + 4 * NSTAGE + 15) & ~15;
+constexpr int SMEM_BYTES = OFF_COMB + HEADS * 8;
 static_assert(SMEM_BYTES <= 232448, "shared memory per block");
+static_assert(4 * 32 * 36 * 4 <= NSTAGE * STAGE_BYTES, "output tiles of the four softmax warps fit the key stages");
 static_assert(KB == 32, "one loader lane per key of a block");
 
 struct MlaArgs {
@@ -105,6 +114,7 @@ struct MlaArgs {
   const uint8_t* resident;  // mode 0: rows for entries -2 - r, or nullptr
   int64_t resident_count;
   float scale_log2;         // sm_scale * log2(e)
+  int32_t nsplit;           // 1 or 2 key halves per request (clusters of 2 * nsplit CTAs)
   float* out;               // [batch][HEADS][DV]
   float* lse;               // [batch][HEADS]
   int32_t* err;
@@ -207,6 +217,14 @@ __device__ __forceinline__ bool bar_wait_cluster(uint64_t* b, unsigned parity, v
   *abort_flag = 1;
   return false;
 }
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void st_peer_v2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -262,6 +280,52 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Output half of one softmax warp's 32 heads: out[h][c] = w0 * O[h][c] (+ w1 * out[h][c], what the CTA of the
+// second key half left there, wherever that head's w1 != 0), O read from tensor memory (zero without it). Each
+// thread holds its head's row; 32-column slices go through a shared tile (rows 144 bytes apart: conflict-free
+// 16-byte accesses both ways) so that the global reads and writes are whole 128-byte row segments.
+__device__ __forceinline__ void store_out_rows(uint32_t trow, bool have_o, float w0, float w1, float* tile,
+                                               float* rows, int lane) {
+  constexpr int TS = 36;  // tile row stride in floats
+  const bool merge = __any_sync(0xffffffffu, w1 != 0.f);
+  const int col4 = lane & 7;
+  for (int c0 = 0; c0 < DV_HALF; c0 += 32) {
+    float o[32];
+    if (have_o) {
+      tmem_ld16(trow + TMEM_O + c0, *reinterpret_cast<float(*)[16]>(o));
+      tmem_ld16(trow + TMEM_O + c0 + 16, *reinterpret_cast<float(*)[16]>(o + 16));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4*>(tile + lane * TS + 4 * q) =
+          make_float4(o[4 * q] * w0, o[4 * q + 1] * w0, o[4 * q + 2] * w0, o[4 * q + 3] * w0);
+    __syncwarp();
+    float4 v[8], o1[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int hl = 4 * r + (lane >> 3);
+      v[r] = *reinterpret_cast<const float4*>(tile + hl * TS + 4 * col4);
+      if (merge) o1[r] = __ldcg(reinterpret_cast<const float4*>(rows + (size_t)hl * DV + c0 + 4 * col4));
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int hl = 4 * r + (lane >> 3);
+      const float w1h = __shfl_sync(0xffffffffu, w1, hl);
+      if (merge && w1h != 0.f) {
+        v[r].x += w1h * o1[r].x;
+        v[r].y += w1h * o1[r].y;
+        v[r].z += w1h * o1[r].z;
+        v[r].w += w1h * o1[r].w;
+      }
+      *reinterpret_cast<float4*>(rows + (size_t)hl * DV + c0 + 4 * col4) = v[r];
+    }
+    __syncwarp();
+  }
+}
+
 // Address of the row an index names, or nullptr for padding / out-of-range entries (masked keys).
 __device__ __forceinline__ const uint8_t* row_of(const MlaArgs& a, int b, int32_t e) {
   if (e >= 0) return e < a.limit ? a.rows + (size_t)b * (size_t)a.req_stride + (size_t)e * ROW_BYTES : nullptr;
@@ -277,9 +341,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.x >> 1, half = blockIdx.x & 1;  // half = rank in the request's cluster of two
-  const uint32_t peer = (uint32_t)(half ^ 1);
-  const int k = a.k, nb = (k + KB - 1) / KB;
+  // cluster of 2 * nsplit CTAs per request: rank = 2 * split + half; split s takes the s-th run of key blocks,
+  // half the score-GEMM columns, and the pair of a split exchanges partial scores
+  const uint32_t rank = cluster_rank();
+  const int b = blockIdx.x / (2 * a.nsplit), half = (int)(rank & 1u), split = (int)(rank >> 1);
+  const uint32_t peer = rank ^ 1u;
+  const int k = a.k, nb_all = (k + KB - 1) / KB, nb_split = (nb_all + a.nsplit - 1) / a.nsplit;
+  const int jb = min(nb_all, split * nb_split);  // this split's first block
+  const int nb = min(nb_all, jb + nb_split) - jb;  // and its block count (the blocks below are numbered from jb)
   // this CTA's score-GEMM columns: [d0, d0 + 8 * nch)
   const int d0 = half ? DSPLIT : 0, nch = (half ? DQK - DSPLIT : DSPLIT) / 8, grp = (nch + 1) * 128;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -320,6 +389,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     bar_init(drain, 1);
     *abort_flag = 0;
     for (int i = 0; i < NSTAGE; ++i) stage_stop[i] = 0;
+    // no key of the second half until its CTA says otherwise (it writes after the first cluster barrier)
+    float2* comb = reinterpret_cast<float2*>(smem + OFF_COMB);
+    for (int i = 0; i < HEADS; ++i) comb[i] = make_float2(-INFINITY, 0.f);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // blocks 0 and 1 of the peer's partial scores are expected in exchange buffers 0 and 1
     bar_arrive_expect(xfull + 0, X_BYTES);
@@ -338,6 +410,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   cluster_sync();  // both CTAs' barriers exist before either touches the other's shared memory
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  // softmax state of head h = tid (warps 0-3), kept for the merge of the key halves after the role loops
+  const int h = tid;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  // this warp's 32 heads of the output half, and a shared tile for writing them (the key stages are free by then)
+  float* const orows = a.out + ((size_t)b * HEADS + (warp & 3) * 32) * DV + half * DV_HALF;
+  float* const otile = reinterpret_cast<float*>(smem + OFF_K) + (warp & 3) * 32 * 36;
+  float m_run = -INFINITY, l_run = 0.f;
+  bool sm_ok = false;
 
   if (warp >= LOAD_WARP0 && warp < XCHG_WARP) {
     // ---- loaders: the STAGE_WARPS warps of stage s fill it with blocks s, s + NSTAGE, ... (this CTA's columns
@@ -352,7 +432,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
         bool ok = j < NSTAGE ||
                   __all_sync(0xffffffffu, bar_wait(kempty + s, (unsigned)((j / NSTAGE) - 1) & 1u, abort_flag));
         if (ok) {
-          const int i = j * KB + lane;
+          const int i = (jb + j) * KB + lane;
           keyp[s * KB + lane] = i < k ? row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i)) : nullptr;
         } else if (lane == 0) {
           stage_stop[s] = 1;
@@ -374,8 +454,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       cp_async_commit();
       if (sub == 0) {
         // this CTA's part of the rows of the stage's next block starts for L2 while these copies land
-        const int i2 = (j + NSTAGE) * KB + lane;
-        if (i2 < k) {
+        const int i2 = (jb + j + NSTAGE) * KB + lane;
+        if (j + NSTAGE < nb && i2 < k) {
           const uint8_t* r2 = row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i2));
           if (r2) prefetch_l2(r2 + d0 * 2, (uint32_t)nch * 16u);
         }
@@ -473,9 +553,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     // ---- softmax: thread h = head h = TMEM lane h. The partial scores of a block go to the peer, whose partial
     //      scores come back; both CTAs then hold S = own + peer (the same value in both, addition commutes) and
     //      run the same softmax, so their P, running max and normaliser agree bit for bit.
-    const int h = tid;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
       const int s = j % NSTAGE, sb = j & 1, xb = j & 1;
@@ -568,30 +645,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       bar_arrive(pfull + pb);
     }
     if (ok && nb > 0) ok = __all_sync(0xffffffffu, bar_wait(odone, 0, abort_flag));
-    if (ok) {
+    sm_ok = ok;
+    if (ok && split == 1) {
+      // second key half: its normalised output goes to `out` (this CTA's columns), and (m, l) of every head to the
+      // CTA of the first half with the same columns, which merges them after the cluster barrier below
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      float* orow = a.out + ((size_t)b * HEADS + h) * DV + half * DV_HALF;
-      for (int c = 0; c < DV_HALF; c += 16) {
-        float o[16];
-        if (nb > 0) {
-          tmem_ld16(trow + TMEM_O + c, o);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4*>(orow + c + i) = make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
-      }
-      if (half == 0)
-        a.lse[(size_t)b * HEADS + h] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      store_out_rows(trow, nb > 0, l_run > 0.f ? 1.f / l_run : 0.f, 0.f, otile, orows, lane);
+      st_peer_v2(peer_addr(smem + OFF_COMB + h * 8, rank - 2u), m_run, l_run);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer no longer writes into this CTA's shared memory
+  cluster_sync();  // the peers no longer touch this CTA's shared memory, and the second half's outputs are written
+  if (warp < SOFTMAX_WARPS && sm_ok && split == 0) {
+      // merge with the second key half (none: m1 = -inf, l1 = 0): with M = max(m0, m1) and c_s = 2^(m_s - M),
+      // out = (c0 O0 + c1 l1 out1) / (c0 l0 + c1 l1), lse = ln 2 * (M + log2(c0 l0 + c1 l1))
+      tc_fence_after();
+      const float2 ml1 = *reinterpret_cast<const float2*>(smem + OFF_COMB + h * 8);
+      const float m1 = a.nsplit > 1 ? ml1.x : -INFINITY, l1 = a.nsplit > 1 ? ml1.y : 0.f;
+      const float mx = fmaxf(m_run, m1);
+      const float c0 = l_run > 0.f ? ex2_approx(m_run - mx) : 0.f, c1 = l1 > 0.f ? ex2_approx(m1 - mx) : 0.f;
+      const float lsum = c0 * l_run + c1 * l1;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      store_out_rows(trow, nb > 0, c0 * inv, c1 * l1 * inv, otile, orows, lane);
+      if (half == 0)
+        a.lse[(size_t)b * HEADS + h] = lsum > 0.f ? (mx + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+  }
+  tc_fence_before();
+  __syncthreads();  // the merge has read the tensor memory
   if (warp == MMA_WARP) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
@@ -599,22 +681,56 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   if (tid == 0 && *abort_flag) atomicOr(a.err, HS_DEVERR_TIMEOUT);
 }
 
-int launch_mla(hs_pool* p, int32_t batch, const MlaArgs& a, cudaStream_t s) {
+// How many clusters of four CTAs (a request's two key halves) the current device holds at once, cached per device.
+int four_cta_clusters_resident() {
+  static std::atomic<int> cache[64];  // 0: not yet asked, else the count + 1
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int c = cache[dev].load(std::memory_order_relaxed);
+  if (c) return c - 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(4, 1, 1);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 4;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, hs_mla_decode_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[dev].store(n + 1, std::memory_order_relaxed);
+  return n;
+}
+
+int launch_mla(hs_pool* p, int32_t batch, MlaArgs a, cudaStream_t s) {
   if (cudaFuncSetAttribute(hs_mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess) {
     cudaGetLastError();
     return HS_ERR_UNSUPPORTED;
   }
+  // Split each request's keys in two (a cluster of four CTAs) when every request's cluster fits on the device at
+  // once; the per-block chain of dependent steps, not a bandwidth, bounds a CTA pair, so twice the SMs take half
+  // the blocks each.
+  a.nsplit = four_cta_clusters_resident() >= batch ? 2 : 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(2 * batch), 1, 1);
+  cfg.gridDim = dim3((unsigned)(2 * a.nsplit * batch), 1, 1);
   cfg.blockDim = dim3(NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;  // the two CTAs of a request
-  attr[1].val.clusterDim.x = 2;
+  attr[1].id = cudaLaunchAttributeClusterDimension;  // the CTAs of a request
+  attr[1].val.clusterDim.x = (unsigned)(2 * a.nsplit);
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;

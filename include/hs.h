@@ -213,8 +213,12 @@ int hs_gather_history(hs_pool *pool, int32_t layer, int32_t batch, const int32_t
  * NULL for none), as hs_resolve_tiered writes them; -1 and anything else is padding. q: device bf16
  * [batch][128][576], 16-byte aligned; out: device fp32 [batch][128][512], 16-byte aligned; lse: device fp32
  * [batch][128]. With no valid entry a head's output is zero and its lse -inf. P is rounded to bf16 before the
- * value product and the normaliser sums the rounded weights; scores and outputs accumulate in fp32. Enqueued on
- * `stream`; batch == 0 or k == 0 is a no-op.
+ * value product and the normaliser sums the rounded weights; scores and outputs accumulate in fp32. When the
+ * device holds a cluster of four CTAs for every request at once, each request's keys are split in two halves
+ * whose softmaxes are merged at the end, with `out` holding the second half's partial output in between: out
+ * must not overlap q, the slot list or the rows. Results are deterministic for a given batch size; a split and
+ * an unsplit launch round differently, within the same error bound. Enqueued on `stream`; batch == 0 or k == 0
+ * is a no-op.
  */
 int hs_mla_decode(hs_pool *pool, int32_t layer, int32_t batch, const void *q, const int32_t *out_slots, int32_t k,
                   const void *resident_rows, int64_t resident_count, float sm_scale, float *out, float *lse,

@@ -105,6 +105,65 @@ def test_decode_after_resolve_matches_history_and_oracle(k, pad):
     assert hs.hs_get_error(buf.handle) == 0
 
 
+def test_decode_large_batch_one_pair_per_request():
+    """Up to the number of four-CTA clusters the device holds at once, a request's keys are split in two and the
+    halves merged (the batches above); a larger batch runs one CTA pair over all of a request's keys. Both agree
+    with the oracle, and the slot-list and history reads stay bit-identical."""
+    w = _w("mla_wide", 52, requests=48, ctx=2048, topk=200, slots=800, steps=2)
+    sel_all = wl.gen_selections(w)[:, 0]
+    rng = np.random.default_rng(52)
+    buf = make_pool(w, noio=True)
+    host = buf.host.numpy().reshape(w.requests, w.ctx, w.row_bytes)
+    q_bits = wl.gen_queries(w.requests, H, DQK, w.seed)
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda()
+    B = w.requests
+    vstats = _value_stats(host)
+    out_slots = torch.empty((B, w.topk), dtype=torch.int32, device="cuda")
+    for s in range(w.steps):
+        sel = sel_all[s].copy()
+        sel[rng.random(sel.shape) < 0.05] = -1
+        sel[5, :] = -1  # a request with nothing valid
+        topk = torch.from_numpy(sel).cuda()
+        hs.hs_step_begin(buf.handle)
+        hs.hs_resolve(buf.handle, 0, B, topk, w.topk, out_slots)
+        out_a, lse_a, out_b, lse_b = _run_pair(buf, q, out_slots, topk, w.topk, SCALE)
+        assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b), s
+        ref_out, ref_lse = _oracle(w, host, q_bits, sel, SCALE)
+        _check(out_a.cpu().numpy(), lse_a.cpu().numpy(), ref_out, ref_lse, vstats, f"wide step {s}")
+        assert not out_a[5].any() and torch.isneginf(lse_a[5]).all()
+    assert hs.hs_get_error(buf.handle) == 0
+
+
+def test_decode_full_size_sampled():
+    """The benchmark's configuration (32 requests, contexts of 131072 rows, top-k 2048 from 4096 hot slots, the
+    same launch as the timed one): every request's slot-list read equals its history read bit for bit, and a
+    sample of requests equals the oracle."""
+    w = wl.WORKLOADS["mla"]
+    sel_all = wl.gen_selections(w, steps=2)[:, 0]
+    buf = make_pool(w)
+    host = buf.host.numpy().reshape(w.requests, w.ctx, w.row_bytes)
+    q_bits = wl.gen_queries(w.requests, H, DQK, w.seed)
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda()
+    B, k = w.requests, w.topk
+    out_slots = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    sample = [0, 13, B - 1]
+    for s in range(2):
+        topk = torch.from_numpy(sel_all[s]).cuda()
+        hs.hs_step_begin(buf.handle)
+        hs.hs_resolve(buf.handle, 0, B, topk, k, out_slots)
+        out_a, lse_a, out_b, lse_b = _run_pair(buf, q, out_slots, topk, k, SCALE)
+        assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b), s
+        sel = sel_all[s][sample]
+        rows = np.zeros((len(sample), k, DQK), dtype=np.uint16)
+        valid = (sel >= 0) & (sel < w.ctx)
+        for i, b in enumerate(sample):
+            rows[i][valid[i]] = host[b][sel[i][valid[i]]].view(np.uint16).reshape(-1, DQK)
+        ref_out, ref_lse = mla.decode_batch(q_bits[sample], rows, valid, SCALE)
+        vstats = _value_stats(rows[valid].view(np.uint8))
+        _check(out_a[sample].cpu().numpy(), lse_a[sample].cpu().numpy(), ref_out, ref_lse, vstats, f"full step {s}")
+    assert hs.hs_get_error(buf.handle) == 0
+
+
 def test_decode_peaked_scores_rescale_path():
     """sm_scale = 1 spreads the scores over hundreds of log2 units, so the running maximum rises by more than 8
     many times and the output accumulator is rescaled in tensor memory; padding rows and a request with no valid
