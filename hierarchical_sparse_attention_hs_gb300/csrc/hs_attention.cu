@@ -249,6 +249,23 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// Score MMAs K0 .. K1-1 of a block (16 columns each, K1 - K0 even). The tensor pipe takes few instructions ahead,
+// so every instruction of the issuing loop shows up in the MMA rate: a loop with a run-time count and the
+// descriptor arithmetic per MMA ran at 46 ns per MMA, this one at about 31 (the rate of the MMA itself). Two MMAs
+// per iteration rather than the whole sequence unrolled: the fully unrolled issue code made the softmax warps of
+// some SMs twice as slow (instruction fetch), the same on every launch.
+template <int K0, int K1>
+__device__ __forceinline__ void issue_qk(uint32_t dst, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  static_assert((K1 - K0) % 2 == 0, "two MMAs per iteration");
+  uint64_t a = a_desc + (uint64_t)(16 * K0), b = b_desc + (uint64_t)(16 * K0);
+#pragma unroll 1
+  for (int kk = K0; kk < K1; kk += 2) {
+    mma_bf16(dst, a, b, idesc, kk != 0 ? 1u : 0u);
+    mma_bf16(dst, a + 16, b + 16, idesc, 1u);
+    a += 32;
+    b += 32;
+  }
+}
 __device__ __forceinline__ void mma_commit(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b))
                : "memory");
@@ -487,16 +504,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       const uint32_t q0 = su32(smem + OFF_Q), k0 = su32(smem + OFF_K), p0 = su32(smem + OFF_P);
       constexpr uint32_t ID_QK = idesc_bf16(128, KB, 0, 0);
       constexpr uint32_t ID_PV = idesc_bf16(128, DV_HALF, 0, 1);
-      const int nk = nch / 2, quarter = nk / 4;  // MMAs of the score GEMM (16 columns each), in four parts
       // Descriptors are built once; an operand 256 bytes further along is the same descriptor plus 16 in its start
-      // field (shared-memory addresses stay below 256 KB, so the 14-bit field never carries), which keeps the
-      // issue loop to a few instructions per MMA.
+      // field (shared-memory addresses stay below 256 KB, so the 14-bit field never carries).
       const uint64_t dq = sdesc(q0, 128, grp), dk = sdesc(k0, 128, grp), dp = sdesc(p0, 128, P_GROUP),
                      dv = sdesc(k0, grp, 128);
       bool ok = true;
-      // The value GEMM of block j-1 goes in as soon as its P is ready: pfull is polled between quarters of the
-      // score GEMM of block j (the tensor pipe runs in issue order), so the key stage of block j-1 is released
-      // without waiting for all of block j's scores.
+      // The value GEMM of block j-1 goes in as soon as its P is ready: pfull is polled halfway through the score
+      // GEMM of block j (the tensor pipe runs in issue order), so the key stage of block j-1 is released without
+      // waiting for all of block j's scores.
       auto issue_pv = [&](int jp) {
         const int s = jp % NSTAGE, pb = jp % NPB;
         tc_fence_after();
@@ -522,19 +537,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
           tc_fence_after();
           const uint64_t dkb = dk + (uint64_t)((s * STAGE_BYTES) >> 4);
           const uint32_t dst = tmem + TMEM_S + sb * KB;
-          uint64_t a_desc = dq, b_desc = dkb;
-#pragma unroll 1
-          for (int q4 = 0; q4 < 4; ++q4) {
-            for (int kq = 0; kq < quarter; ++kq) {
-              mma_bf16(dst, a_desc, b_desc, ID_QK, (q4 | kq) != 0);
-              a_desc += 16;  // the next 16 columns: 256 bytes further along
-              b_desc += 16;
-            }
-            if (pv_pending && bar_poll(pfull + jp % NPB, (unsigned)(jp / NPB) & 1u)) {
-              issue_pv(jp);
-              pv_pending = false;
-            }
+          constexpr int NK0 = DSPLIT / 16, NK1 = (DQK - DSPLIT) / 16;  // score MMAs of CTA 0 and CTA 1
+          if (half == 0)
+            issue_qk<0, NK0 / 2>(dst, dq, dkb, ID_QK);
+          else
+            issue_qk<0, NK1 / 2>(dst, dq, dkb, ID_QK);
+          if (pv_pending && bar_poll(pfull + jp % NPB, (unsigned)(jp / NPB) & 1u)) {
+            issue_pv(jp);
+            pv_pending = false;
           }
+          if (half == 0)
+            issue_qk<NK0 / 2, NK0>(dst, dq, dkb, ID_QK);
+          else
+            issue_qk<NK1 / 2, NK1>(dst, dq, dkb, ID_QK);
           mma_commit(sfull + sb);
         }
         if (pv_pending) {
