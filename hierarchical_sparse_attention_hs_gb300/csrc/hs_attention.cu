@@ -386,6 +386,51 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     cp_async16(smem + OFF_Q + g * grp + c * 128 + (h & 7) * 16, qsrc + (size_t)h * ROW_BYTES + c * 16);
   }
   cp_async_commit();
+
+  // Loaders: the STAGE_WARPS warps of stage s fill it with blocks s, s + NSTAGE, ... (this CTA's columns of each
+  // row). The stage's first warp looks up the block's 32 rows (lane i: key i) into the stage's row pointers, a
+  // named barrier hands them to the other warps, every thread copies its share of the 16-byte chunks, and the first
+  // warp starts the stage's next rows on their way into L2. Each stage's first block is started here, alongside
+  // Q, before anything waits, and lands before the barrier below; the L2 prefetches of those stages' next blocks
+  // wait until after it, so that they do not compete with the first copies.
+  const bool loader = warp >= LOAD_WARP0 && warp < XCHG_WARP;
+  const int ls = (warp - LOAD_WARP0) / STAGE_WARPS, lsub = (warp - LOAD_WARP0) % STAGE_WARPS;
+  uint8_t* const lst = smem + OFF_K + ls * STAGE_BYTES;
+  auto load_rows = [&](int j) {
+    if (lsub == 0) {
+      const int i = (jb + j) * KB + lane;
+      keyp[ls * KB + lane] = i < k ? row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i)) : nullptr;
+    }
+    named_sync(1 + ls, STAGE_WARPS * 32);
+  };
+  auto prefetch_next = [&](int j) {
+    if (lsub == 0) {
+      // this CTA's part of the rows of the stage's next block starts for L2 while these copies land
+      const int i2 = (jb + j + NSTAGE) * KB + lane;
+      if (j + NSTAGE < nb && i2 < k) {
+        const uint8_t* r2 = row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i2));
+        if (r2) prefetch_l2(r2 + d0 * 2, (uint32_t)nch * 16u);
+      }
+    }
+  };
+  auto copy_rows = [&](int j) {
+    // thread order walks the shared-memory layout (8 rows of one chunk, then the next chunk), so a warp's copies
+    // fill consecutive 16-byte slots
+    for (int e = lsub * 32 + lane; e < KB * nch; e += STAGE_WARPS * 32) {
+      const int g = e / (8 * nch), rem = e - g * 8 * nch, c = rem >> 3, r = g * 8 + (rem & 7);
+      uint8_t* dst = lst + g * grp + c * 128 + (r & 7) * 16;
+      const uint8_t* src = keyp[ls * KB + r];
+      if (src)
+        cp_async16(dst, src + d0 * 2 + c * 16);
+      else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_commit();
+  };
+  if (loader && ls < nb) {
+    load_rows(ls);
+    copy_rows(ls);
+  }
   if (tid == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
       bar_init(kfull + i, STAGE_WARPS * 32);
@@ -406,14 +451,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     bar_init(drain, 1);
     *abort_flag = 0;
     for (int i = 0; i < NSTAGE; ++i) stage_stop[i] = 0;
-    // no key of the second half until its CTA says otherwise (it writes after the first cluster barrier)
-    float2* comb = reinterpret_cast<float2*>(smem + OFF_COMB);
-    for (int i = 0; i < HEADS; ++i) comb[i] = make_float2(-INFINITY, 0.f);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // blocks 0 and 1 of the peer's partial scores are expected in exchange buffers 0 and 1
     bar_arrive_expect(xfull + 0, X_BYTES);
     bar_arrive_expect(xfull + 1, X_BYTES);
   }
+  // no key of the second half until its CTA says otherwise (it writes after the first cluster barrier)
+  if (tid < HEADS) reinterpret_cast<float2*>(smem + OFF_COMB)[tid] = make_float2(-INFINITY, 0.f);
   if (warp == MMA_WARP) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tslot)),
                  "r"(TMEM_COLS)
@@ -436,50 +480,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   float m_run = -INFINITY, l_run = 0.f;
   bool sm_ok = false;
 
-  if (warp >= LOAD_WARP0 && warp < XCHG_WARP) {
-    // ---- loaders: the STAGE_WARPS warps of stage s fill it with blocks s, s + NSTAGE, ... (this CTA's columns
-    //      of each row): the stage's first warp waits until the value GEMM of the block NSTAGE earlier has read
-    //      the stage and looks up the 32 rows (lane i: key i), a named barrier releases the other warps, every
-    //      thread copies its share of the 16-byte chunks, and each signals the stage full as its copies land.
-    //      The stop decision is read after the barrier, so the stage's threads leave the loop together.
-    const int ws = warp - LOAD_WARP0, s = ws / STAGE_WARPS, sub = ws % STAGE_WARPS;
-    uint8_t* st = smem + OFF_K + s * STAGE_BYTES;
-    for (int j = s; j < nb; j += NSTAGE) {
-      if (sub == 0) {
-        bool ok = j < NSTAGE ||
-                  __all_sync(0xffffffffu, bar_wait(kempty + s, (unsigned)((j / NSTAGE) - 1) & 1u, abort_flag));
-        if (ok) {
-          const int i = (jb + j) * KB + lane;
-          keyp[s * KB + lane] = i < k ? row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i)) : nullptr;
-        } else if (lane == 0) {
-          stage_stop[s] = 1;
+  if (loader) {
+    // ---- loaders (see above): the first block of each stage has landed; later blocks wait until the value GEMM
+    //      of the block NSTAGE earlier has read the stage. The stop decision is read after the named barrier, so
+    //      the stage's threads leave the loop together.
+    if (ls < nb) {
+      bar_arrive(kfull + ls);
+      prefetch_next(ls);
+    }
+    for (int j = ls + NSTAGE; j < nb; j += NSTAGE) {
+      if (lsub == 0) {
+        const bool ok = __all_sync(0xffffffffu, bar_wait(kempty + ls, (unsigned)((j / NSTAGE) - 1) & 1u, abort_flag));
+        if (!ok && lane == 0) stage_stop[ls] = 1;
+        if (!ok) {
+          named_sync(1 + ls, STAGE_WARPS * 32);
+          break;
         }
       }
-      named_sync(1 + s, STAGE_WARPS * 32);
-      if (stage_stop[s]) break;
-      // thread order walks the shared-memory layout (8 rows of one chunk, then the next chunk), so a warp's
-      // copies fill consecutive 16-byte slots
-      for (int e = sub * 32 + lane; e < KB * nch; e += STAGE_WARPS * 32) {
-        const int g = e / (8 * nch), rem = e - g * 8 * nch, c = rem >> 3, r = g * 8 + (rem & 7);
-        uint8_t* dst = st + g * grp + c * 128 + (r & 7) * 16;
-        const uint8_t* src = keyp[s * KB + r];
-        if (src)
-          cp_async16(dst, src + d0 * 2 + c * 16);
-        else
-          *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      cp_async_commit();
-      if (sub == 0) {
-        // this CTA's part of the rows of the stage's next block starts for L2 while these copies land
-        const int i2 = (jb + j + NSTAGE) * KB + lane;
-        if (j + NSTAGE < nb && i2 < k) {
-          const uint8_t* r2 = row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i2));
-          if (r2) prefetch_l2(r2 + d0 * 2, (uint32_t)nch * 16u);
-        }
-      }
+      load_rows(j);
+      if (stage_stop[ls]) break;
+      copy_rows(j);
+      prefetch_next(j);
       cp_async_wait_all();
       fence_proxy_async();
-      bar_arrive(kfull + s);
+      bar_arrive(kfull + ls);
     }
     cp_async_wait_all();
   } else if (warp == XCHG_WARP) {
