@@ -18,10 +18,11 @@
 // commutes), run the same softmax, and each multiplies P by its own value half (columns 0..255 or 256..511, which
 // lie within its columns). Half of Q per CTA leaves room for four key stages, and no score work is repeated.
 // A request's keys are split in two as well (two pairs, a cluster of four CTAs) whenever every request's cluster
-// fits on the device at once: each pair runs the softmax over its half of the key blocks, the second pair writes
-// its normalised output half to `out` and its (max, normaliser) per head into the first pair's shared memory, and
-// after a cluster barrier the first pair merges the two (flash-decoding's split-K merge, inside one cluster). A
-// pair's time is a chain of dependent steps per key block, not a bandwidth, so two pairs per request halve it.
+// fits on the device at once: each pair runs the softmax over its half of the key blocks, and each merges half of
+// the heads (flash-decoding's split-K merge, inside one cluster): for the other heads a pair writes its normalised
+// output to `out` and its (max, normaliser) per head into the other pair's shared memory, and after a cluster
+// barrier merges its own heads with what the other pair left. A pair's time is a chain of dependent steps per key
+// block, not a bandwidth, so two pairs per request halve it.
 // Warp roles per CTA:
 //   warps 0-3   softmax: thread h owns head h, which is TMEM lane h of the score and output accumulators;
 //   warp 4      lane 0 issues every tcgen05.mma (and warp 4 allocates / frees the tensor memory);
@@ -92,11 +93,11 @@ constexpr int OFF_P = OFF_K + NSTAGE * STAGE_BYTES;
 constexpr int OFF_X = OFF_P + NPB * P_BYTES;       // two exchange buffers
 constexpr int OFF_KEY = OFF_X + 2 * X_BYTES;       // row pointers of each stage: [NSTAGE][KB]
 // mbarriers: kfull[NSTAGE] kempty[NSTAGE] sfull[2] sempty[2] pfull[NPB] pdone[NPB] odone drain xfull[2] xempty[2]
-// xread[2]
-constexpr int NBAR = 2 * NSTAGE + 4 + 2 * NPB + 2 + 6;
+// xread[2] tdone
+constexpr int NBAR = 2 * NSTAGE + 4 + 2 * NPB + 2 + 6 + 1;
 constexpr int OFF_BAR = OFF_KEY + NSTAGE * KB * 8;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM address, abort flag, per-stage stop flags
-// (m, l) of every head from the CTA that ran the second key half, when a request's keys are split
+// (m, l) per head from the CTA of the other key half, for the heads this CTA merges
 constexpr int OFF_COMB = (OFF_MISC + 8 + 4 * NSTAGE + 15) & ~15;
 constexpr int SMEM_BYTES = OFF_COMB + HEADS * 8;
 static_assert(SMEM_BYTES <= 232448, "shared memory per block");
@@ -298,7 +299,7 @@ __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sy
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Output half of one softmax warp's 32 heads: out[h][c] = w0 * O[h][c] (+ w1 * out[h][c], what the CTA of the
-// second key half left there, wherever that head's w1 != 0), O read from tensor memory (zero without it). Each
+// other key half left there, wherever that head's w1 != 0), O read from tensor memory (zero without it). Each
 // thread holds its head's row; 32-column slices go through a shared tile (rows 144 bytes apart: conflict-free
 // 16-byte accesses both ways) so that the global reads and writes are whole 128-byte row segments.
 __device__ __forceinline__ void store_out_rows(uint32_t trow, bool have_o, float w0, float w1, float* tile,
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t *kfull = bars, *kempty = bars + NSTAGE, *sfull = bars + 2 * NSTAGE, *sempty = sfull + 2,
            *pfull = sempty + 2, *pdone = pfull + NPB, *odone = pdone + NPB, *drain = odone + 1, *xfull = drain + 1,
-           *xempty = xfull + 2, *xread = xempty + 2;
+           *xempty = xfull + 2, *xread = xempty + 2, *tdone = xread + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   volatile int* stage_stop = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
@@ -449,6 +450,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     }
     bar_init(odone, 1);
     bar_init(drain, 1);
+    bar_init(tdone, SOFTMAX_WARPS * 32);  // every softmax thread has made its last tensor-memory read
     *abort_flag = 0;
     for (int i = 0; i < NSTAGE; ++i) stage_stop[i] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -479,6 +481,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   float* const otile = reinterpret_cast<float*>(smem + OFF_K) + (warp & 3) * 32 * 36;
   float m_run = -INFINITY, l_run = 0.f;
   bool sm_ok = false;
+  // with two key halves, the CTA of half s merges heads 64 s .. 64 s + 63 (softmax warps 2 s and 2 s + 1) and
+  // hands the other heads to its counterpart
+  const bool merges = a.nsplit == 1 || (warp >> 1) == split;
 
   if (loader) {
     // ---- loaders (see above): the first block of each stage has landed; later blocks wait until the value GEMM
@@ -685,20 +690,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     }
     if (ok && nb > 0) ok = __all_sync(0xffffffffu, bar_wait(odone, 0, abort_flag));
     sm_ok = ok;
-    if (ok && split == 1) {
-      // second key half: its normalised output goes to `out` (this CTA's columns), and (m, l) of every head to the
-      // CTA of the first half with the same columns, which merges them after the cluster barrier below
+    if (ok && !merges) {
+      // heads the other key half merges: this half's normalised output goes to `out` (this CTA's columns), and
+      // (m, l) to the CTA of the other half with the same columns
       tc_fence_after();
       store_out_rows(trow, nb > 0, l_run > 0.f ? 1.f / l_run : 0.f, 0.f, otile, orows, lane);
-      st_peer_v2(peer_addr(smem + OFF_COMB + h * 8, rank - 2u), m_run, l_run);
+      st_peer_v2(peer_addr(smem + OFF_COMB + h * 8, rank ^ 2u), m_run, l_run);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the peers no longer touch this CTA's shared memory, and the second half's outputs are written
-  if (warp < SOFTMAX_WARPS && sm_ok && split == 0) {
-      // merge with the second key half (none: m1 = -inf, l1 = 0): with M = max(m0, m1) and c_s = 2^(m_s - M),
+  if (warp < SOFTMAX_WARPS && sm_ok && merges) {
+      // merge with the other key half (none: m1 = -inf, l1 = 0): with M = max(m0, m1) and c_s = 2^(m_s - M),
       // out = (c0 O0 + c1 l1 out1) / (c0 l0 + c1 l1), lse = ln 2 * (M + log2(c0 l0 + c1 l1))
       tc_fence_after();
       const float2 ml1 = *reinterpret_cast<const float2*>(smem + OFF_COMB + h * 8);
@@ -711,13 +716,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       if (half == 0)
         a.lse[(size_t)b * HEADS + h] = lsum > 0.f ? (mx + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
   }
-  tc_fence_before();
-  __syncthreads();  // the merge has read the tensor memory
+  // The tensor memory is freed once every softmax thread has arrived on tdone after its last read of it (a
+  // per-thread arrival count: a CTA-wide bar.sync here was seen to let the other warps through while two warps
+  // were still in the merge, so it does not order the free after those reads). The wait is bounded but does not
+  // stop at the abort flag: aborted threads skip their reads and arrive at once.
+  if (warp < SOFTMAX_WARPS) {
+    tc_fence_before();
+    bar_arrive(tdone);
+  }
   if (warp == MMA_WARP) {
+    if (lane == 0) {
+      for (unsigned it = 0; it < WAIT_LIMIT && !bar_test(tdone, 0); ++it) {
+      }
+      if (*abort_flag) atomicOr(a.err, HS_DEVERR_TIMEOUT);
+    }
+    __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
   }
-  if (tid == 0 && *abort_flag) atomicOr(a.err, HS_DEVERR_TIMEOUT);
 }
 
 // How many clusters of four CTAs (a request's two key halves) the current device holds at once, cached per device.
