@@ -156,6 +156,32 @@ def captured_traffic(w: wl.Workload, cold_launches: int, steady_launches: int):
     return (cold_launches * d["cold"] + steady_launches * d["steady"]) / n if n else None
 
 
+def attention_sources_sha16() -> str:
+    """Hash of the files the attention kernel is compiled from, which its committed ncu capture must match."""
+    import hashlib
+
+    from hierarchical_sparse_attention_hs_gb300 import build as hs_build
+
+    csrc = os.path.join(os.path.dirname(hs_build.__file__), "csrc")
+    files = [os.path.join(csrc, n) for n in ("hs_attention.cu", "hs_pool.hpp")]
+    parts = [hashlib.sha256(open(f, "rb").read()).hexdigest() for f in files]
+    return hashlib.sha256("".join(parts).encode()).hexdigest()[:16]
+
+
+def captured_attention_traffic(w: wl.Workload):
+    """DRAM bytes per launch of the attention kernel from its committed ncu capture on this workload, when the
+    kernel sources are the ones it was taken on; else None."""
+    path = os.path.join(ROOT, "profiles", f"hs_mla_decode_kernel_{w.name}_ncu.json")
+    try:
+        with open(path) as f:
+            cap = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if cap.get("attention_sources_sha16") != attention_sources_sha16():
+        return None
+    return cap["dram_read_bytes"] + cap["dram_write_bytes"]
+
+
 def meta_bytes_per_launch(w: wl.Workload, batch: int) -> int:
     """Metadata bytes of one resolve launch that do not depend on hits/misses: selection read, tok2slot gather,
     out_slots write (4k each) and the stamp + slot-token reads (8H), per request-layer."""
@@ -727,9 +753,12 @@ def run_gpu(args) -> int:
             "kernel": "hs_mla_decode_kernel", "bound": "tensor", "achieved": tflops, "peak": bf16_peak,
             "unit": "TFLOP/s", "frac": tflops / bf16_peak, "ms_per_launch": a["ms"], "ms_per_launch_p50": a["ms_p50"],
             "flops_per_launch": a["flops"], "valid_rows_per_launch": a["valid_rows"],
-            "flops_definition": "2 * 128 heads * valid rows * (576 + 512): the score and value products that "
-                                "are needed (the kernel also recomputes the scores in its second value half)",
-            "row_bytes_per_launch": 2 * a["valid_rows"] * w.row_bytes,
+            "flops_definition": "2 * 128 heads * valid rows * (576 + 512): the score and value products; no "
+                                "score work is repeated (each CTA of a pair computes the scores over its own columns)",
+            "row_bytes_per_launch": a["valid_rows"] * w.row_bytes,
+            "traffic": captured_attention_traffic(w),
+            "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed ncu capture "
+                              "(profiles/), null unless taken on these kernel sources",
             "peak_source": "bf16_tflops (cuBLAS bf16 GEMM, burst) in MEASURED_PEAKS.json" if "bf16_tflops" in peaks
                            else "fallback 1900 TFLOP/s",
             "timing": "CUDA events around one graph launch each, L2 flushed before each, on the launch stream",
