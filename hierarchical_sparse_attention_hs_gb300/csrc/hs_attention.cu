@@ -96,9 +96,10 @@ constexpr int OFF_KEY = OFF_X + 2 * X_BYTES;       // row pointers of each stage
 // xread[2] tdone
 constexpr int NBAR = 2 * NSTAGE + 4 + 2 * NPB + 2 + 6 + 1;
 constexpr int OFF_BAR = OFF_KEY + NSTAGE * KB * 8;
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM address, abort flag, per-stage stop flags
+// TMEM address, abort flag, per-stage stop flags, per-stage masks of the keys with a row
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 // (m, l) per head from the CTA of the other key half, for the heads this CTA merges
-constexpr int OFF_COMB = (OFF_MISC + 8 + 4 * NSTAGE + 15) & ~15;
+constexpr int OFF_COMB = (OFF_MISC + 8 + 8 * NSTAGE + 15) & ~15;
 constexpr int SMEM_BYTES = OFF_COMB + HEADS * 8;
 static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 static_assert(4 * 32 * 36 * 4 <= NSTAGE * STAGE_BYTES, "output tiles of the four softmax warps fit the key stages");
@@ -376,6 +377,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   volatile int* stage_stop = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
+  uint32_t* kmask = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 8 + 4 * NSTAGE);  // bit i: key i has a row
   const uint8_t** keyp = reinterpret_cast<const uint8_t**>(smem + OFF_KEY);
 
   // this CTA's columns of Q: head h, columns d0 + 8c .. d0 + 8c + 7 at (h/8)*grp + c*128 + (h%8)*16; thread
@@ -400,7 +402,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   auto load_rows = [&](int j) {
     if (lsub == 0) {
       const int i = (jb + j) * KB + lane;
-      keyp[ls * KB + lane] = i < k ? row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i)) : nullptr;
+      const uint8_t* r = i < k ? row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i)) : nullptr;
+      keyp[ls * KB + lane] = r;
+      const uint32_t m = __ballot_sync(0xffffffffu, r != nullptr);
+      if (lane == 0) kmask[ls] = m;
     }
     named_sync(1 + ls, STAGE_WARPS * 32);
   };
@@ -631,15 +636,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
         sv[4 * g + 3] += o.w;
       }
       bar_arrive(xread + xb);  // the exchange warp hands the buffer back to the peer
-      // the stage's row pointers (written by the loaders before they signalled the stage full)
+      // which keys of the block have a row (written by the loaders before they signalled the stage full)
       ok = __all_sync(0xffffffffu, bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag));
       if (!ok) break;
-      const uint8_t* const* kp = keyp + s * KB;
+      const uint32_t vm = kmask[s];
       float x[KB];
       float mb = -INFINITY;
 #pragma unroll
       for (int i = 0; i < KB; ++i) {
-        x[i] = kp[i] ? sv[i] * a.scale_log2 : -INFINITY;
+        x[i] = (vm >> i) & 1u ? sv[i] * a.scale_log2 : -INFINITY;
         mb = fmaxf(mb, x[i]);
       }
       float m_new = m_run;
@@ -667,11 +672,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       float psum = 0.f;
 #pragma unroll
       for (int i = 0; i < KB / 2; ++i) {
-        const __nv_bfloat16 lo = __float2bfloat16_rn(x[2 * i] == -INFINITY ? 0.f : ex2_approx(x[2 * i] - m_run));
-        const __nv_bfloat16 hi =
-            __float2bfloat16_rn(x[2 * i + 1] == -INFINITY ? 0.f : ex2_approx(x[2 * i + 1] - m_run));
-        psum += __bfloat162float(lo) + __bfloat162float(hi);
-        pk[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+        // both weights rounded to bf16 by one conversion (key 2i in the low half)
+        const __nv_bfloat162 p2 =
+            __floats2bfloat162_rn(x[2 * i] == -INFINITY ? 0.f : ex2_approx(x[2 * i] - m_run),
+                                  x[2 * i + 1] == -INFINITY ? 0.f : ex2_approx(x[2 * i + 1] - m_run));
+        const float2 pf = __bfloat1622float2(p2);
+        psum += pf.x + pf.y;
+        pk[i] = *reinterpret_cast<const uint32_t*>(&p2);
       }
       l_run += psum;
       // P buffer pb is free once the value GEMM of block j - NPB has read it
