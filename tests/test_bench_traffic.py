@@ -1,0 +1,47 @@
+"""bench.py's traffic bookkeeping on CPU: a committed ncu capture counts only while the kernel sources it was taken
+on are unchanged (the hash it records matches), otherwise the bench line reports null."""
+import json
+
+import bench
+import workload as wl
+
+
+def _write(tmp_path, name, payload):
+    prof = tmp_path / "profiles"
+    prof.mkdir(exist_ok=True)
+    (prof / name).write_text(json.dumps(payload))
+
+
+def test_attention_traffic_follows_the_source_hash(tmp_path, monkeypatch):
+    w = wl.WORKLOADS["mla"]
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.captured_attention_traffic(w) is None  # no capture at all
+    good = {"attention_sources_sha16": bench.attention_sources_sha16(), "dram_read_bytes": 1000,
+            "dram_write_bytes": 24}
+    _write(tmp_path, f"hs_mla_decode_kernel_{w.name}_ncu.json", good)
+    assert bench.captured_attention_traffic(w) == 1024
+    _write(tmp_path, f"hs_mla_decode_kernel_{w.name}_ncu.json", dict(good, attention_sources_sha16="0" * 16))
+    assert bench.captured_attention_traffic(w) is None  # taken on other sources
+
+
+def test_resolve_traffic_weights_cold_and_steady_launches(tmp_path, monkeypatch):
+    w = wl.WORKLOADS["dsa"]
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    cap = {"kernel_sources_sha16": bench.kernel_sources_sha16(), "dram_bytes_per_launch": {"cold": 900, "steady": 100}}
+    _write(tmp_path, f"hs_resolve_kernel_{w.name}_ncu.json", cap)
+    assert bench.captured_traffic(w, 1, 3) == (900 + 3 * 100) / 4
+    _write(tmp_path, f"hs_resolve_kernel_{w.name}_ncu.json", dict(cap, kernel_sources_sha16="f" * 16))
+    assert bench.captured_traffic(w, 1, 3) is None
+
+
+def test_committed_captures_name_their_sources():
+    """Each committed capture records the hash of the sources it was taken on, and its command runs committed
+    files only."""
+    import os
+
+    for name in ("hs_resolve_kernel_dsa_ncu.json", "hs_mla_decode_kernel_mla_ncu.json"):
+        cap = json.load(open(os.path.join(bench.ROOT, "profiles", name)))
+        key = "kernel_sources_sha16" if name.startswith("hs_resolve") else "attention_sources_sha16"
+        assert len(cap[key]) == 16 and int(cap[key], 16) >= 0
+        assert cap["command"].startswith("ncu ") and "--clock-control none" in cap["command"]
+        assert "_work" not in cap["command"]
