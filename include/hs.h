@@ -215,8 +215,8 @@ int hs_gather_history(hs_pool *pool, int32_t layer, int32_t batch, const int32_t
  * [batch][128]. With no valid entry a head's output is zero and its lse -inf. P is rounded to bf16 before the
  * value product and the normaliser sums the rounded weights; scores and outputs accumulate in fp32. When the
  * device holds a cluster of four CTAs for every request at once, each request's keys are split in two halves
- * whose softmaxes are merged at the end, with `out` holding the second half's partial output in between: out
- * must not overlap q, the slot list or the rows. Results are deterministic for a given batch size; a split and
+ * whose softmaxes are merged at the end, with `out` holding the halves' partial outputs in between: out must not
+ * overlap q, the slot list or the rows. Results are deterministic for a given batch size; a split and
  * an unsplit launch round differently, within the same error bound. Enqueued on `stream`; batch == 0 or k == 0
  * is a no-op.
  */
