@@ -239,8 +239,14 @@ def test_decode_argument_errors():
     with pytest.raises(hs.HsError) as e:
         hs.hs_mla_decode_history(buf2.handle, 0, 1, q, idx, 8, SCALE, out, lse)
     assert e.value.code == hs.HS_ERR_UNSUPPORTED
+    out.fill_(7.0)
+    lse.fill_(7.0)
     hs.hs_mla_decode(buf.handle, 0, 0, q, idx, 32, None, 0, SCALE, out, lse)  # batch 0: no-op
+    hs.hs_mla_decode(buf.handle, 0, 2, q, idx, 0, None, 0, SCALE, out, lse)  # k 0: no-op
+    hs.hs_mla_decode_history(buf.handle, 0, 2, q, idx, 0, SCALE, out, lse)
     torch.cuda.synchronize()
+    assert bool((out == 7.0).all()) and bool((lse == 7.0).all())  # nothing written
+    assert hs.hs_get_error(buf.handle) == 0
 
 
 def test_decode_history_from_host_memory():
