@@ -22,7 +22,7 @@ __all__ = [
     "hs_pool_destroy", "hs_host_alloc", "hs_host_free", "hs_error_string", "HS_DEVERR_RANGE", "HS_DEVERR_DUP",
     "HS_DEVERR_STATE", "HostBuffer", "PoolBuffers", "hs_probe_link", "hs_gather", "hs_gather_history",
     "hs_resolve_shared", "hs_resolve_tiered", "hs_mla_decode", "hs_mla_decode_history", "HS_DEVERR_TIMEOUT",
-    "MLA_HEADS", "MLA_D_QK", "MLA_D_V",
+    "MLA_HEADS", "MLA_D_QK", "MLA_D_V", "hs_probe_launch", "hs_debug_attention",
 ]
 
 HS_OK = 0
@@ -94,6 +94,8 @@ def load():
             "hs_host_free": (ctypes.c_int, [vp]),
             "hs_error_string": (ctypes.c_char_p, [ctypes.c_int]),
             "hs_probe_link": (ctypes.c_int, [vp, vp, sz, i32, vp, P(ctypes.c_double), P(ctypes.c_double)]),
+            "hs_probe_launch": (ctypes.c_int, [vp, i32, i32, i32, i32, vp]),
+            "hs_debug_attention": (ctypes.c_int, [ctypes.c_uint32, i32, P(i32)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -132,6 +134,18 @@ def hs_probe_link(host_ptr: int, dev, nbytes: int, iters: int = 5, stream=None) 
     _check(load().hs_probe_link(host_ptr, _addr(dev), nbytes, iters, _stream(stream), ctypes.byref(zc),
                                 ctypes.byref(cp)), "hs_probe_link")
     return zc.value, cp.value
+
+
+def hs_probe_launch(pool: int, layer: int, nlayers: int, batch: int, k: int, stream=None) -> None:
+    _check(load().hs_probe_launch(pool, layer, nlayers, batch, k, _stream(stream)), "hs_probe_launch")
+
+
+def hs_debug_attention(wait_limit: int = 0, stall: bool = False) -> int:
+    """Test hook: set the attention kernel's wait limit (0 = default) and stall switch; returns the largest batch
+    whose keys are split over two CTA pairs on the current device."""
+    n = ctypes.c_int32()
+    _check(load().hs_debug_attention(wait_limit, int(bool(stall)), ctypes.byref(n)), "hs_debug_attention")
+    return int(n.value)
 
 
 def hs_error_string(code: int) -> str:

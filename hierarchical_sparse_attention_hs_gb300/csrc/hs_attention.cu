@@ -120,6 +120,8 @@ struct MlaArgs {
   float* out;               // [batch][HEADS][DV]
   float* lse;               // [batch][HEADS]
   int32_t* err;
+  uint32_t wait_limit;      // polling rounds before a role's wait gives up (WAIT_LIMIT unless a test lowers it)
+  int32_t stall;            // test hook: the issuer first waits on a barrier that nothing completes
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -167,10 +169,11 @@ __device__ __forceinline__ bool bar_poll(uint64_t* b, unsigned parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase of the given parity; false once the abort flag is set or after WAIT_LIMIT rounds (which
-// sets it).
-__device__ __forceinline__ bool bar_wait(uint64_t* b, unsigned parity, volatile int* abort_flag) {
-  for (unsigned it = 0; it < WAIT_LIMIT; ++it) {
+// Wait for the phase of the given parity; false once the abort flag is set or after `limit` rounds (which sets
+// it).
+__device__ __forceinline__ bool bar_wait(uint64_t* b, unsigned parity, volatile int* abort_flag,
+                                         unsigned limit = WAIT_LIMIT) {
+  for (unsigned it = 0; it < limit; ++it) {
     if (bar_test(b, parity)) return true;
     if (*abort_flag) return false;
   }
@@ -204,8 +207,9 @@ __device__ __forceinline__ void bar_arrive_peer(uint32_t addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 // a wait whose arrivals come from the peer (cluster-scope acquire makes its stores visible)
-__device__ __forceinline__ bool bar_wait_cluster(uint64_t* b, unsigned parity, volatile int* abort_flag) {
-  for (unsigned it = 0; it < WAIT_LIMIT; ++it) {
+__device__ __forceinline__ bool bar_wait_cluster(uint64_t* b, unsigned parity, volatile int* abort_flag,
+                                                 unsigned limit) {
+  for (unsigned it = 0; it < limit; ++it) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
@@ -489,6 +493,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   // with two key halves, the CTA of half s merges heads 64 s .. 64 s + 63 (softmax warps 2 s and 2 s + 1) and
   // hands the other heads to its counterpart
   const bool merges = a.nsplit == 1 || (warp >> 1) == split;
+  const unsigned lim = a.wait_limit;
 
   if (loader) {
     // ---- loaders (see above): the first block of each stage has landed; later blocks wait until the value GEMM
@@ -500,7 +505,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     }
     for (int j = ls + NSTAGE; j < nb; j += NSTAGE) {
       if (lsub == 0) {
-        const bool ok = __all_sync(0xffffffffu, bar_wait(kempty + ls, (unsigned)((j / NSTAGE) - 1) & 1u, abort_flag));
+        const bool ok = __all_sync(0xffffffffu, bar_wait(kempty + ls, (unsigned)((j / NSTAGE) - 1) & 1u, abort_flag, lim));
         if (!ok && lane == 0) stage_stop[ls] = 1;
         if (!ok) {
           named_sync(1 + ls, STAGE_WARPS * 32);
@@ -523,7 +528,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     if (lane == 0) {
       for (int j = 0; j < nb; ++j) {
         const int xb = j & 1;
-        if (!bar_wait(xread + xb, (unsigned)(j >> 1) & 1u, abort_flag)) break;
+        if (!bar_wait(xread + xb, (unsigned)(j >> 1) & 1u, abort_flag, lim)) break;
         if (j + 2 < nb) {
           bar_arrive_expect(xfull + xb, X_BYTES);
           bar_arrive_peer(peer_addr(xempty + xb, peer));
@@ -542,7 +547,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       // field (shared-memory addresses stay below 256 KB, so the 14-bit field never carries).
       const uint64_t dq = sdesc(q0, 128, grp), dk = sdesc(k0, 128, grp), dp = sdesc(p0, 128, P_GROUP),
                      dv = sdesc(k0, grp, 128);
-      bool ok = true;
+      // test hook: wait on a barrier that nothing completes (drain: its only arrival is the commit below), before
+      // anything is issued, so that the wait runs out with no tensor-core work or copy of this CTA in flight
+      bool ok = !a.stall || bar_wait(drain, 0, abort_flag, lim);
       // The value GEMM of block j-1 goes in as soon as its P is ready: pfull is polled halfway through the score
       // GEMM of block j (the tensor pipe runs in issue order), so the key stage of block j-1 is released without
       // waiting for all of block j's scores.
@@ -565,8 +572,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
         const int jp = j - 1;
         if (j < nb) {
           const int s = j % NSTAGE, sb = j & 1;
-          ok = bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag);
-          if (ok && j >= 2) ok = bar_wait(sempty + sb, (unsigned)((j - 2) >> 1) & 1u, abort_flag);
+          ok = bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag, lim);
+          if (ok && j >= 2) ok = bar_wait(sempty + sb, (unsigned)((j - 2) >> 1) & 1u, abort_flag, lim);
           if (!ok) break;
           tc_fence_after();
           const uint64_t dkb = dk + (uint64_t)((s * STAGE_BYTES) >> 4);
@@ -587,15 +594,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
           mma_commit(sfull + sb);
         }
         if (pv_pending) {
-          ok = bar_wait(pfull + jp % NPB, (unsigned)(jp / NPB) & 1u, abort_flag);
+          ok = bar_wait(pfull + jp % NPB, (unsigned)(jp / NPB) & 1u, abort_flag, lim);
           if (!ok) break;
           issue_pv(jp);
         }
       }
       // every issued MMA has finished before the tensor memory is freed
       mma_commit(drain);
-      for (unsigned it = 0; it < WAIT_LIMIT && !bar_test(drain, 0); ++it) {
+      bool drained = false;
+      for (unsigned it = 0; it < WAIT_LIMIT && !(drained = bar_test(drain, 0)); ++it) {
       }
+      if (!drained) *abort_flag = 1;
     }
     __syncwarp();
   } else {
@@ -605,7 +614,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
       const int s = j % NSTAGE, sb = j & 1, xb = j & 1;
-      ok = __all_sync(0xffffffffu, ok && bar_wait(sfull + sb, (unsigned)(j >> 1) & 1u, abort_flag));
+      ok = __all_sync(0xffffffffu, ok && bar_wait(sfull + sb, (unsigned)(j >> 1) & 1u, abort_flag, lim));
       if (!ok) break;
       tc_fence_after();
       float sv[KB];
@@ -615,7 +624,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       bar_arrive(sempty + sb);
       // the exchange buffer xb of the peer is free once the peer has read block j - 2 from it
       if (j >= 2) {
-        ok = __all_sync(0xffffffffu, bar_wait_cluster(xempty + xb, (unsigned)((j - 2) >> 1) & 1u, abort_flag));
+        ok = __all_sync(0xffffffffu, bar_wait_cluster(xempty + xb, (unsigned)((j - 2) >> 1) & 1u, abort_flag, lim));
         if (!ok) break;
       }
       // exchange buffer layout: float4 group g (scores 4g..4g+3) of head h at (g * HEADS + h) * 16; the stores
@@ -625,7 +634,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
 #pragma unroll
       for (int g = 0; g < KB / 4; ++g)
         st_peer_async_v4(xpeer + g * HEADS * 16, sv[4 * g], sv[4 * g + 1], sv[4 * g + 2], sv[4 * g + 3], xfull_peer);
-      ok = __all_sync(0xffffffffu, bar_wait_cluster(xfull + xb, (unsigned)(j >> 1) & 1u, abort_flag));
+      ok = __all_sync(0xffffffffu, bar_wait_cluster(xfull + xb, (unsigned)(j >> 1) & 1u, abort_flag, lim));
       if (!ok) break;
 #pragma unroll
       for (int g = 0; g < KB / 4; ++g) {
@@ -637,7 +646,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       }
       bar_arrive(xread + xb);  // the exchange warp hands the buffer back to the peer
       // which keys of the block have a row (written by the loaders before they signalled the stage full)
-      ok = __all_sync(0xffffffffu, bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag));
+      ok = __all_sync(0xffffffffu, bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag, lim));
       if (!ok) break;
       const uint32_t vm = kmask[s];
       float x[KB];
@@ -653,7 +662,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       if (__any_sync(0xffffffffu, resc)) {
         // O holds blocks 0 .. j-1 once the value GEMM of block j-1 has finished; scale this warp's rows
         ok = __all_sync(0xffffffffu,
-                        bar_wait(pdone + ((j - 1) % NPB), (unsigned)((j - 1) / NPB) & 1u, abort_flag));
+                        bar_wait(pdone + ((j - 1) % NPB), (unsigned)((j - 1) / NPB) & 1u, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
         const float f = resc ? ex2_approx(m_run - m_new) : 1.f;
@@ -684,7 +693,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       // P buffer pb is free once the value GEMM of block j - NPB has read it
       const int pb = j % NPB;
       if (j >= NPB) {
-        ok = __all_sync(0xffffffffu, bar_wait(pdone + pb, (unsigned)((j - NPB) / NPB) & 1u, abort_flag));
+        ok = __all_sync(0xffffffffu, bar_wait(pdone + pb, (unsigned)((j - NPB) / NPB) & 1u, abort_flag, lim));
         if (!ok) break;
       }
       uint8_t* prow = smem + OFF_P + pb * P_BYTES + (h >> 3) * P_GROUP + (h & 7) * 16;
@@ -695,7 +704,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       tc_fence_before();
       bar_arrive(pfull + pb);
     }
-    if (ok && nb > 0) ok = __all_sync(0xffffffffu, bar_wait(odone, 0, abort_flag));
+    if (ok && nb > 0) ok = __all_sync(0xffffffffu, bar_wait(odone, 0, abort_flag, lim));
     sm_ok = ok;
     if (ok && !merges) {
       // heads the other key half merges: this half's normalised output goes to `out` (this CTA's columns), and
@@ -733,8 +742,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   }
   if (warp == MMA_WARP) {
     if (lane == 0) {
-      for (unsigned it = 0; it < WAIT_LIMIT && !bar_test(tdone, 0); ++it) {
+      bool done = false;
+      for (unsigned it = 0; it < WAIT_LIMIT && !(done = bar_test(tdone, 0)); ++it) {
       }
+      if (!done) *abort_flag = 1;  // a softmax thread never arrived: report it like any other wait that ran out
       if (*abort_flag) atomicOr(a.err, HS_DEVERR_TIMEOUT);
     }
     __syncwarp();
@@ -773,6 +784,10 @@ int four_cta_clusters_resident() {
   return n;
 }
 
+// Failure-detection test settings (hs_debug_attention_waits): the role-wait limit and the stall hook.
+std::atomic<unsigned> g_wait_limit{WAIT_LIMIT};
+std::atomic<int> g_stall{0};
+
 int launch_mla(hs_pool* p, int32_t batch, MlaArgs a, cudaStream_t s) {
   if (cudaFuncSetAttribute(hs_mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess) {
@@ -783,6 +798,8 @@ int launch_mla(hs_pool* p, int32_t batch, MlaArgs a, cudaStream_t s) {
   // once; the per-block chain of dependent steps, not a bandwidth, bounds a CTA pair, so twice the SMs take half
   // the blocks each.
   a.nsplit = four_cta_clusters_resident() >= batch ? 2 : 1;
+  a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  a.stall = g_stall.load(std::memory_order_relaxed);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * a.nsplit * batch), 1, 1);
   cfg.blockDim = dim3(NTHREADS, 1, 1);
@@ -857,4 +874,11 @@ extern "C" int hs_mla_decode_history(hs_pool* pool, int32_t layer, int32_t batch
   a.lse = lse;
   a.err = pool->err;
   return launch_mla(pool, batch, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int hs_debug_attention(uint32_t wait_limit, int32_t stall, int32_t* split_max_batch) {
+  g_wait_limit.store(wait_limit ? wait_limit : WAIT_LIMIT, std::memory_order_relaxed);
+  g_stall.store(stall ? 1 : 0, std::memory_order_relaxed);
+  if (split_max_batch) *split_max_batch = four_cta_clusters_resident();
+  return HS_OK;
 }

@@ -63,7 +63,11 @@ constexpr int MAX_CLUSTER = HS_MAX_CLUSTER;
 constexpr int GA_WARPS = NW / 2;                 // group A: miss ranks and the first wave of row loads
 constexpr int GA_THREADS = GA_WARPS * 32;
 constexpr int BITMAP_MAX_CTX = 1 << 18;          // longer contexts rank misses with the radix sort
-constexpr int MISC_BAD = 0, MISC_NCAND = 1, MISC_CBUF = 2, MISC_NEXT = 3, MISC_NINP = 4, MISC_INTS = 5;
+constexpr int MISC_BAD = 0, MISC_NCAND = 1, MISC_NEXT = 2, MISC_NINP = 3, MISC_XFAIL = 4, MISC_INTS = 5;
+constexpr int NBUCKET = 2048;  // miss ranking: tokens are counted into at most this many buckets of 2^shift
+constexpr int XROW = 36;       // victim choice: one warp's row = 32 stamp counts + (min, max, count, 0) stamps
+constexpr int XROWS = MAX_CLUSTER * (NW - GA_WARPS);  // rows of the exchange table: every warp of group B
+constexpr unsigned XWAIT_LIMIT = 1u << 22;  // polls of an exchange barrier before the call is given up
 
 struct ResolveArgs {
   const int32_t* topk;           // [batch][k]
@@ -97,7 +101,8 @@ __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(
 
 // Shared-memory carve-up, identical on host and device.
 struct SmemLayout {
-  size_t sel, slot, stamp, stok, hit, mpos, cidx, mscr, mscr2, mscr3, tbl, red, wstat, misc, total;
+  size_t sel, slot, stamp, stok, hit, mpos, cidx, mscr, rank, bcnt, blist, vic, xrow, bar, tbl, red, wstat, misc,
+      total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int k, int slots, int ctx) {
@@ -110,16 +115,16 @@ __host__ __device__ inline SmemLayout smem_layout(int k, int slots, int ctx) {
   L.hit = o;   o = align16(o + sizeof(uint32_t) * ((slots + 31) / 32));
   L.mpos = o;  o = align16(o + sizeof(uint16_t) * k);
   L.cidx = o;  o = align16(o + sizeof(uint16_t) * 2 * slots);
-  if (use_bitmap(ctx)) {
-    const size_t words = ((size_t)ctx + 31) / 32;
-    L.mscr = o;  o = align16(o + sizeof(uint32_t) * words);   // token bitmap
-    L.mscr2 = o; o = align16(o + sizeof(uint16_t) * words);   // misses below each word
-    L.mscr3 = o;
-  } else {
-    L.mscr = o;  o = align16(o + sizeof(uint16_t) * 2 * k);   // radix ping-pong
-    L.mscr2 = o; o = align16(o + sizeof(uint16_t) * k);       // rank of each miss position
-    L.mscr3 = o;
-  }
+  if (use_bitmap(ctx))
+    L.mscr = o, o = align16(o + sizeof(uint32_t) * (((size_t)ctx + 31) / 32));  // token bitmap
+  else
+    L.mscr = o, o = align16(o + sizeof(uint16_t) * 2 * k);  // radix ping-pong (repeated in-place tokens)
+  L.rank = o;  o = align16(o + sizeof(uint16_t) * k);         // rank of the miss at each selection entry
+  L.bcnt = o;  o = align16(o + sizeof(int32_t) * NBUCKET);    // misses per token bucket, then bucket bounds
+  L.blist = o; o = align16(o + sizeof(int32_t) * k);          // miss tokens grouped by bucket
+  L.vic = o;   o = align16(o + sizeof(int32_t) * k);          // victim j, the slot of the miss of rank j
+  L.xrow = o;  o = align16(o + sizeof(int32_t) * XROWS * XROW);
+  L.bar = o;   o = align16(o + sizeof(uint64_t) * 2);          // exchange barriers: rows, victims
   L.tbl = o;   o = align16(o + sizeof(int32_t) * NW * TBL_STRIDE);
   L.red = o;   o = align16(o + sizeof(int32_t) * 2 * RED_INTS);
   L.wstat = o; o = align16(o + sizeof(int32_t) * 4 * NW);
@@ -166,11 +171,54 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Every warp executes these as a whole (the .aligned forms).
+// Every warp executes these as a whole (the .aligned forms). The arrive carries no release: it signals that
+// this CTA's reads of the shared metadata have returned their values (loads consumed, copies waited for), which
+// no later write of another CTA can change; there is nothing of this CTA's to publish at that point.
 __device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Exchanges between the CTAs of a cluster through distributed shared memory: asynchronous remote stores whose
+// bytes complete the transaction count of the receiver's mbarrier, which the receiver waits on.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, int cta) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(cta));
+  return r;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+// the one local arrival, announcing the bytes the phase waits for
+__device__ __forceinline__ void mbar_expect(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void st_async_v4(uint32_t addr, int x, int y, int z, int w, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.s32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_s32(uint32_t addr, int x, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.s32 [%0], %1, [%2];" ::"r"(addr), "r"(x),
+               "r"(bar)
+               : "memory");
+}
+// Wait for phase 0 of an exchange barrier (cluster-scope acquire: the remote bytes are visible afterwards); false
+// if it did not complete within XWAIT_LIMIT polls.
+__device__ __forceinline__ bool mbar_wait0(uint64_t* b) {
+  for (unsigned it = 0; it < XWAIT_LIMIT; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], 0;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(b))
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
 
 // Walk a chunk sequence c, c + S, c + 2S, ... as (row, chunk-in-row) pairs without a division per step.
 struct ChunkWalk {
@@ -209,12 +257,15 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   int* s_wval = s_whi + NW;
   int* s_wmiss = s_wval + NW;
   int* s_misc = reinterpret_cast<int*>(smem + L.misc);
-  // bitmap ranking
-  uint32_t* s_bits = reinterpret_cast<uint32_t*>(smem + L.mscr);
-  uint16_t* s_below = reinterpret_cast<uint16_t*>(smem + L.mscr2);
-  // radix ranking
-  uint16_t* s_mbuf = reinterpret_cast<uint16_t*>(smem + L.mscr);
-  uint16_t* s_rank = reinterpret_cast<uint16_t*>(smem + L.mscr2);
+  uint32_t* s_bits = reinterpret_cast<uint32_t*>(smem + L.mscr);   // token bitmap (short contexts)
+  uint16_t* s_mbuf = reinterpret_cast<uint16_t*>(smem + L.mscr);   // sort buffers (long contexts)
+  uint16_t* s_rank = reinterpret_cast<uint16_t*>(smem + L.rank);
+  int32_t* s_bcnt = reinterpret_cast<int32_t*>(smem + L.bcnt);
+  int32_t* s_blist = reinterpret_cast<int32_t*>(smem + L.blist);
+  int32_t* s_vic = reinterpret_cast<int32_t*>(smem + L.vic);
+  int32_t* s_xrow = reinterpret_cast<int32_t*>(smem + L.xrow);
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + L.bar);
+  uint64_t* vbar = xbar + 1;
 
   // Programmatic dependent launch: wait until the preceding kernel in the stream has completed and its writes
   // are visible, then let the next kernel start its launch while this one runs.
@@ -276,7 +327,17 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   for (int w = tid; w < hwords; w += NT) s_hit[w] = 0u;
   if (BITMAP)
     for (int w = tid; w < cwords; w += NT) s_bits[w] = 0u;
+  for (int x = tid; x < NBUCKET; x += NT) s_bcnt[x] = 0;
+  if (tid == 0) {
+    mbar_init(xbar, 1);
+    mbar_init(vbar, 1);
+    if (C > 1) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // every row of group B of every CTA of the cluster lands here (when there are misses to place)
+    mbar_expect(xbar, (uint32_t)(C * (NW - GA_WARPS) * XROW * 4));
+  }
   __syncthreads();
+  // the exchange barriers exist before any CTA of the cluster sends to them (waited for after step 3)
+  if (C > 1) cluster_arrive();
 
   // 2. hit test over this warp's run of entries: hits mark their slot, misses their token
   int nvalid = 0, nmiss = 0;
@@ -337,8 +398,6 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   }
   cp_async_wait_all();
   __syncthreads();
-  // Every read of the cluster-shared metadata by this CTA has completed.
-  if (C > 1) cluster_arrive();
 
   // 3. the misses in selection order (the same list in every CTA of the cluster)
   int m = 0, run = 0;
@@ -356,6 +415,10 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     run += __popc(bal);
   }
   __syncthreads();
+  if (C > 1) {
+    cluster_wait();    // every CTA of the cluster runs, its exchange barriers initialised
+    cluster_arrive();  // every read of the cluster-shared metadata by this CTA has returned its value
+  }
   const int nchunk = m * cpr;  // 16-byte chunks of the rows; chunk c = chunk c % cpr of miss c / cpr
   const int nblk = (nchunk + BLK - 1) / BLK;
   // Blocks go to the CTAs in runs of RUN consecutive blocks (whole rows when rows span several blocks): run s
@@ -382,38 +445,55 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
         cw.next();
       }
     }
-    if (BITMAP && m > 0) {
-      const int seg = (cwords + GA_WARPS - 1) / GA_WARPS;
-      const int beg = min(cwords, warp * seg);
-      const int end = min(cwords, beg + seg);
-      int c = 0;
-      for (int w = beg + lane; w < end; w += 32) c += __popc(s_bits[w]);
-      c = __reduce_add_sync(0xffffffffu, c);
-      if (lane == 0) red[warp] = c;
+    if (m > 0) {
+      // Rank of each miss among the misses by token, by a counting sort on the token's top bits: tokens fall into
+      // at most NBUCKET buckets of 2^shift consecutive tokens; a miss's rank is the number of misses in earlier
+      // buckets plus the smaller tokens in its own bucket (a handful); an equal token there is a repeat.
+      const int shift = max(0, bits_of((unsigned)(ctx - 1)) - 11);
+      for (int q = g.tid(); q < m; q += GA_THREADS) atomicAdd(&s_bcnt[s_sel[s_mpos[q]] >> shift], 1);
       g.sync();
-      int below = 0;
-      for (int w = 0; w < GA_WARPS; ++w) below += w < warp ? red[w] : 0;
-      for (int base = beg; base < end; base += 32) {
-        const int w = base + lane;
-        const int p = w < end ? __popc(s_bits[w]) : 0;
-        int incl = p;
+      // buckets of this thread: a contiguous run of NBUCKET / 256 (all buckets are scanned: the unused ones
+      // past nbk stay zero)
+      constexpr int PER = NBUCKET / GA_THREADS;
+      static_assert(PER % 4 == 0, "runs of whole 16-byte groups");
+      int4 q4[PER / 4];
+      int c = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        if (w < end) s_below[w] = (uint16_t)(below + incl - p);
-        below += __shfl_sync(0xffffffffu, incl, 31);
+      for (int u = 0; u < PER / 4; ++u) {
+        q4[u] = *reinterpret_cast<const int4*>(s_bcnt + g.tid() * PER + 4 * u);
+        c += q4[u].x + q4[u].y + q4[u].z + q4[u].w;
       }
-    } else if (!BITMAP && m > 0) {
-      int m2 = 0;
-      const uint16_t* order = hs::radix_sort(
-          g, m, bits_of((unsigned)(ctx - 1)), s_mbuf, s_mbuf + k, [&](int q) { return s_sel[s_mpos[q]]; },
-          [](int) { return true; }, s_tbl, red, &m2);
-      for (int j = g.tid(); j < m; j += GA_THREADS) {
-        const int pos = s_mpos[order[j]];
-        s_rank[pos] = (uint16_t)j;
-        if (j && s_sel[pos] == s_sel[s_mpos[order[j - 1]]]) bad |= HS_DEVERR_DUP;
+      int total;
+      int start = hs::group_exclusive_scan(g, c, red, &total);
+#pragma unroll
+      for (int u = 0; u < PER / 4; ++u) {
+        int4 o;
+        o.x = start;
+        o.y = o.x + q4[u].x;
+        o.z = o.y + q4[u].y;
+        o.w = o.z + q4[u].z;
+        start = o.w + q4[u].w;
+        *reinterpret_cast<int4*>(s_bcnt + g.tid() * PER + 4 * u) = o;
+      }
+      g.sync();
+      // the tokens placed bucket by bucket; afterwards s_bcnt[x] is the end of bucket x (the start of x + 1)
+      for (int q = g.tid(); q < m; q += GA_THREADS) {
+        const int t = s_sel[s_mpos[q]];
+        s_blist[atomicAdd(&s_bcnt[t >> shift], 1)] = t;
+      }
+      g.sync();
+      for (int q = g.tid(); q < m; q += GA_THREADS) {
+        const int pos = s_mpos[q];
+        const int t = s_sel[pos], x = t >> shift;
+        const int e = s_bcnt[x];
+        int r = x ? s_bcnt[x - 1] : 0, eq = 0;
+        for (int j = r; j < e; ++j) {
+          const int y = s_blist[j];
+          r += y < t;
+          eq += y == t;
+        }
+        s_rank[pos] = (uint16_t)r;
+        if (eq > 1) bad |= HS_DEVERR_DUP;
       }
     }
     if (!BITMAP && s_misc[MISC_NINP] > 1) {
@@ -429,41 +509,152 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     }
     if (tid == 0) s_misc[MISC_NEXT] = min(GA_WARPS, my_blocks);  // the first wave took blocks [0, this)
   } else {
-    // B: victims in (stamp, slot) order
+    // B: victims in (stamp, slot) order, the m smallest keys among the slots not hit. The CTAs of the cluster
+    //    split the slots: CTA r takes the r-th range, its warp w the w-th part of it, so segment r * 8 + w runs
+    //    in ascending slot order.
     const Group g{GA_WARPS, NW - GA_WARPS, 2};
-    int smin = 0x7fffffff, smax = -1;
-    if (m > 0) {
-      for (int v = g.tid(); v < H; v += g.size()) {
-        smin = min(smin, s_stamp[v]);
-        smax = max(smax, s_stamp[v]);
-      }
-      smin = (int)__reduce_min_sync(0xffffffffu, (unsigned)smin);
-      smax = __reduce_max_sync(0xffffffffu, smax);
-      if (lane == 0) {
-        s_wlo[g.warp()] = smin;
-        s_whi[g.warp()] = smax;
-      }
-      g.sync();
-      for (int w = 0; w < g.nw; ++w) {
-        smin = min(smin, s_wlo[w]);
-        smax = max(smax, s_whi[w]);
-      }
-    }
-    const int stamp_bits = smax >= smin ? bits_of((unsigned)(smax - smin)) : 0;
+    int* red = s_red + RED_INTS;
     int ncand = 0;
-    const uint16_t* cidx = s_cidx;
-    if (m > 0)  // a call whose selection is all resident (a resolve after its prefetch) needs no victims
-      cidx = hs::radix_sort(
-          g, H, stamp_bits, s_cidx, s_cidx + H, [&](int v) { return s_stamp[v] - smin; },
-          [&](int v) { return !(s_hit[v >> 5] & (1u << (v & 31))); }, s_tbl, s_red + RED_INTS, &ncand, m);
-    if (g.tid() == 0) {
-      s_misc[MISC_NCAND] = ncand;
-      s_misc[MISC_CBUF] = cidx == s_cidx ? 0 : 1;
+    if (m > 0) {  // a call whose selection is all resident (a resolve after its prefetch) needs no victims
+      auto cand = [&](int v) { return !(s_hit[v >> 5] & (1u << (v & 31))); };
+      const int hc = ((H + C * g.size() - 1) / (C * g.size())) * g.size();  // slots per CTA
+      const int hw = hc / g.nw;                                             // per warp, a multiple of 32
+      const int sbeg = min(H, rank * hc + g.warp() * hw), send = min(H, sbeg + hw);
+      const int sg = rank * g.nw + g.warp();
+      // lanes of a run of 32 slots whose 5-bit bin is this lane's, from the run's bit planes of the bin
+      auto bin_lanes = [&](unsigned part, unsigned p0, unsigned p1, unsigned p2, unsigned p3, unsigned p4) {
+        return part & ((lane & 1) ? p0 : ~p0) & ((lane & 2) ? p1 : ~p1) & ((lane & 4) ? p2 : ~p2) &
+               ((lane & 8) ? p3 : ~p3) & ((lane & 16) ? p4 : ~p4);
+      };
+      auto planes = [&](bool part, int x) {
+        return bin_lanes(__ballot_sync(0xffffffffu, part), __ballot_sync(0xffffffffu, x & 1),
+                         __ballot_sync(0xffffffffu, x & 2), __ballot_sync(0xffffffffu, x & 4),
+                         __ballot_sync(0xffffffffu, x & 8), __ballot_sync(0xffffffffu, x & 16));
+      };
+      constexpr int U = 4;  // runs of 32 slots in flight per iteration
+      // One pass over the segment: the candidates' stamp range and count, and (lane b) how many have
+      // stamp % 32 == b. Once the range is known to span at most 32 stamps, these are the exact per-stamp counts.
+      int smin = 0x7fffffff, smax = -1, nc = 0, cnt = 0;
+      for (int base = sbeg; base < send; base += 32 * U) {
+        int st[U];
+        bool c[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = base + 32 * u + lane;
+          c[u] = v < send && cand(v);
+          st[u] = c[u] ? s_stamp[v] : 0;
+          if (c[u]) {
+            smin = min(smin, st[u]);
+            smax = max(smax, st[u]);
+            ++nc;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) cnt += __popc(planes(c[u], st[u] & 31));
+      }
+      smin = (int)__reduce_min_sync(0xffffffffu, (unsigned)smin);  // stamps are >= 0
+      smax = __reduce_max_sync(0xffffffffu, smax);
+      nc = __reduce_add_sync(0xffffffffu, nc);
+      // the segment's row goes to row sg of every CTA of the cluster (16-byte pieces, lanes 0-8)
+      {
+        const int p = lane < 8 ? lane : 0;
+        const int x0 = __shfl_sync(0xffffffffu, cnt, 4 * p), x1 = __shfl_sync(0xffffffffu, cnt, 4 * p + 1),
+                  x2 = __shfl_sync(0xffffffffu, cnt, 4 * p + 2), x3 = __shfl_sync(0xffffffffu, cnt, 4 * p + 3);
+        int4 piece = lane < 8 ? make_int4(x0, x1, x2, x3) : make_int4(smin, smax, nc, 0);
+        int32_t* row = s_xrow + sg * XROW + 4 * lane;
+        if (C > 1) {
+          if (lane < XROW / 4)
+            for (int dst = 0; dst < C; ++dst)
+              st_async_v4(cluster_addr(row, dst), piece.x, piece.y, piece.z, piece.w, cluster_addr(xbar, dst));
+          if (!mbar_wait0(xbar)) s_misc[MISC_XFAIL] = 1;
+          g.sync();  // every warp of the group takes the same branch below
+        } else {
+          if (lane < XROW / 4) *reinterpret_cast<int4*>(row) = piece;
+          g.sync();
+        }
+      }
+      const bool xfail = s_misc[MISC_XFAIL] != 0;
+      if (xfail) bad |= HS_DEVERR_TIMEOUT;
+      // the cluster's range and count (every warp reads the rows: lane j takes rows j and j + 32)
+      const int nrows = C * g.nw;
+      int gmin = 0x7fffffff, gmax = -1, gnc = 0;
+#pragma unroll 2
+      for (int j = lane; j < nrows; j += 32) {
+        gmin = min(gmin, s_xrow[j * XROW + 32]);
+        gmax = max(gmax, s_xrow[j * XROW + 33]);
+        gnc += s_xrow[j * XROW + 34];
+      }
+      gmin = (int)__reduce_min_sync(0xffffffffu, (unsigned)gmin);
+      gmax = __reduce_max_sync(0xffffffffu, gmax);
+      gnc = __reduce_add_sync(0xffffffffu, gnc);
+      ncand = gnc;
+      if (m <= gnc && gmax - gmin <= 31 && !xfail) {
+        // Stamp bin d = stamp - gmin < 32, lane d's counts in column (gmin + d) % 32. The bin totals and their
+        // prefix give T, the bin holding position m - 1: bins below T are taken whole, bin T in slot order up to
+        // m, at positions in (bin, segment, slot) order, which is (stamp, slot) order -- ties to the lowest slot.
+        const int col = (gmin + lane) & 31;
+        int before = 0, tot = 0;
+#pragma unroll 8
+        for (int j = 0; j < nrows; ++j) {
+          const int x = s_xrow[j * XROW + col];
+          before += j < sg ? x : 0;
+          tot += x;
+        }
+        int incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        // T exists: every candidate lies in bins 0..31 and there are at least m of them
+        const int T = __ffs(__ballot_sync(0xffffffffu, incl >= m)) - 1;
+        int mybase = incl - tot + before;  // position of this segment's next slot of bin `lane`
+        if (C > 1 && g.tid() == 0) mbar_expect(vbar, (uint32_t)(4 * m));
+        for (int base = sbeg; base < send; base += 32 * U) {
+          int d[U];
+          unsigned mine[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int v = base + 32 * u + lane;
+            d[u] = (v < send && cand(v)) ? s_stamp[v] - gmin : 32;
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) mine[u] = planes(d[u] <= T, d[u]);
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int from = d[u] <= T ? d[u] : 0;
+            const unsigned peers = __shfl_sync(0xffffffffu, mine[u], from);
+            const int at = __shfl_sync(0xffffffffu, mybase, from);
+            if (d[u] <= T) {
+              const int pos = at + __popc(peers & hs::lanemask_lt());
+              if (d[u] < T || pos < m) {
+                const int v = base + 32 * u + lane;
+                if (C > 1)
+                  for (int dst = 0; dst < C; ++dst)
+                    st_async_s32(cluster_addr(s_vic + pos, dst), v, cluster_addr(vbar, dst));
+                else
+                  s_vic[pos] = v;
+              }
+            }
+            mybase += __popc(mine[u]);
+          }
+        }
+        if (C > 1) {
+          if (!mbar_wait0(vbar)) bad |= HS_DEVERR_TIMEOUT;
+        }
+      } else if (m <= gnc && !xfail) {
+        // the candidates span more than 32 stamps: every CTA sorts all of them (stable LSD on stamp - gmin)
+        int n2 = 0;
+        const uint16_t* order = hs::radix_sort(
+            g, H, bits_of((unsigned)(gmax - gmin)), s_cidx, s_cidx + H, [&](int v) { return s_stamp[v] - gmin; },
+            cand, s_tbl, red, &n2, m);
+        for (int j = g.tid(); j < m; j += g.size()) s_vic[j] = order[j];
+      }
     }
+    if (g.tid() == 0) s_misc[MISC_NCAND] = ncand;
   }
   if (bad) atomicOr(&s_misc[MISC_BAD], (int)bad);
   __syncthreads();
-  const uint16_t* cidx = s_cidx + (s_misc[MISC_CBUF] ? H : 0);
   bad = (unsigned)s_misc[MISC_BAD] | (m > s_misc[MISC_NCAND] ? HS_DEVERR_STATE : 0u);
 
   if (bad) {
@@ -475,17 +666,8 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     return;
   }
 
-  // victim of the miss at selection entry i holding token t
-  auto victim_of = [&](int i, int t) -> int {
-    int j;
-    if (BITMAP) {
-      const int w = t >> 5;
-      j = s_below[w] + __popc(s_bits[w] & ((1u << (t & 31)) - 1u));
-    } else {
-      j = s_rank[i];
-    }
-    return cidx[j];
-  };
+  // victim of the miss at selection entry i
+  auto victim_of = [&](int i, int) -> int { return s_vic[s_rank[i]]; };
   auto store_chunk_to = [&](uint8_t* dst_hot, int q, int w, const uint4& val) {
     const int i = s_mpos[q];
     *reinterpret_cast<uint4*>(dst_hot + (size_t)victim_of(i, s_sel[i]) * R + ((size_t)w << 4)) = val;
@@ -530,8 +712,8 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     // A: 5. per owned selection entry, once every CTA of the cluster has read the metadata: hits are
     //    stamped, a miss of rank j takes victim j
     if (C > 1) cluster_wait();
-    for (int i = tid; i < k; i += GA_THREADS) {
-      if (!owned(i)) continue;
+    // this CTA's runs of 32 entries are rank, rank + C, ...: warp w takes runs w, w + 8, ... of them
+    for (int i = (rank + C * warp) * 32 + lane; i < k; i += C * GA_WARPS * 32) {
       const int32_t t = s_sel[i];
       const int32_t s = s_slot[i];
       if (s >= 0) {
@@ -615,6 +797,13 @@ __global__ void hs_gather_kernel(const uint8_t* __restrict__ base, int64_t req_s
       if (c < n) *reinterpret_cast<uint4*>(dst + ((size_t)c << 4)) = v[u];
     }
   }
+}
+
+// Does nothing but take part in programmatic dependent launch: launched with a resolve's exact configuration, it
+// measures the fixed cost of the launch itself (the floor under a resolve step).
+__global__ void __launch_bounds__(NT, 1) hs_empty_kernel(const ResolveArgs) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
 }
 
 __global__ void hs_step_kernel(int32_t* step) {
@@ -737,12 +926,12 @@ int pick_cluster(const hs_pool* p, int batch) {
 
 int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk, int32_t k, int32_t* out,
                    cudaStream_t s, int32_t nlayers = 1, const int32_t* resident = nullptr,
-                   int64_t resident_stride = 0) {
+                   int64_t resident_stride = 0, bool empty = false) {
   if (!p || layer < 0 || nlayers < 1 || layer > p->d.layers - nlayers || batch < 0 || batch > p->d.max_batch ||
       k < 0 || k > p->d.topk_max)
     return HS_ERR_INVALID_ARG;
   if (batch == 0 || k == 0) return HS_OK;
-  if (!topk) return HS_ERR_INVALID_ARG;
+  if (!topk && !empty) return HS_ERR_INVALID_ARG;
   const size_t rl0 = (size_t)layer * (size_t)p->d.max_batch;
   ResolveArgs a;
   a.topk = topk;
@@ -791,7 +980,9 @@ int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk
   cfg.numAttrs = (unsigned)na;
   const bool bm = use_bitmap(p->d.ctx);
   cudaError_t e;
-  if (p->noio)
+  if (empty)
+    e = cudaLaunchKernelEx(&cfg, hs_empty_kernel, a);
+  else if (p->noio)
     e = bm ? cudaLaunchKernelEx(&cfg, hs_resolve_kernel<false, true>, a)
            : cudaLaunchKernelEx(&cfg, hs_resolve_kernel<false, false>, a);
   else
@@ -848,7 +1039,8 @@ int hs_pool_create(const hs_pool_desc* desc, hs_stream_t stream, hs_pool** out) 
       cudaFuncSetAttribute(hs_resolve_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
           cudaSuccess ||
       cudaFuncSetAttribute(hs_resolve_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
-          cudaSuccess)
+          cudaSuccess ||
+      cudaFuncSetAttribute(hs_empty_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
     return HS_ERR_CUDA;
 
   hs_pool* p = new (std::nothrow) hs_pool;
@@ -1027,6 +1219,11 @@ int hs_pool_destroy(hs_pool* pool) {
   if (!pool) return HS_ERR_INVALID_ARG;
   delete pool;
   return HS_OK;
+}
+
+int hs_probe_launch(hs_pool* pool, int32_t layer, int32_t nlayers, int32_t batch, int32_t k, hs_stream_t stream) {
+  return launch_resolve(pool, layer, batch, nullptr, k, nullptr, reinterpret_cast<cudaStream_t>(stream), nlayers,
+                        nullptr, 0, true);
 }
 
 int hs_host_alloc(size_t bytes, void** out) {

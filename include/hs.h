@@ -230,6 +230,20 @@ int hs_mla_decode(hs_pool *pool, int32_t layer, int32_t batch, const void *q, co
 int hs_mla_decode_history(hs_pool *pool, int32_t layer, int32_t batch, const void *q, const int32_t *topk_idx,
                           int32_t k, float sm_scale, float *out, float *lse, hs_stream_t stream);
 
+/*
+ * Test hook of the attention consumer (not for production use; process-wide settings, not thread-safe). It lets a
+ * test exercise failure detection without faulting the GPU: every wait inside the kernel is bounded, and on running
+ * out it stops every role, frees its tensor memory, returns and sets HS_DEVERR_TIMEOUT.
+ *   wait_limit: polling rounds after which a wait of the kernel's roles gives up (0 restores the default, 2^20).
+ *   stall != 0: the tensor-core issuer of every CTA first waits on a barrier that nothing completes, so that wait
+ *     runs out before any tensor-core work or row copy of the kernel is issued, and the abort path runs with
+ *     nothing in flight. 0 restores normal operation.
+ *   split_max_batch: if non-NULL, receives the largest batch for which hs_mla_decode splits a request's keys over
+ *     two CTA pairs on the current device (larger batches run one pair per request).
+ * Applies to the hs_mla_decode / hs_mla_decode_history calls made after it.
+ */
+int hs_debug_attention(uint32_t wait_limit, int32_t stall, int32_t *split_max_batch);
+
 /* Synchronise the device, then read the sticky device error word into *out (HS_DEVERR_* bits); clear it when
  * `clear` is non-zero. */
 int hs_get_error(hs_pool *pool, int32_t *out, int32_t clear);
@@ -253,6 +267,15 @@ int hs_host_free(void *ptr);
  */
 int hs_probe_link(const void *host, void *dev, size_t bytes, int32_t iters, hs_stream_t stream,
                   double *zero_copy_gbs, double *memcpy_gbs);
+
+/*
+ * Measure the fixed cost under a resolve (not for the hot path): enqueue a kernel that does nothing but wait for its
+ * predecessor and release its dependents, launched with exactly the configuration that hs_resolve (nlayers == 1) or
+ * hs_resolve_shared would use for this layer range, batch and k: grid, cluster size, dynamic shared memory and
+ * programmatic dependent launch. A decode step made of these launches in place of the resolves times the floor that
+ * launching alone puts under the step. Argument checks as hs_resolve_shared; touches no memory; capturable.
+ */
+int hs_probe_launch(hs_pool *pool, int32_t layer, int32_t nlayers, int32_t batch, int32_t k, hs_stream_t stream);
 
 /* Static text for an HS_ERR_* code. */
 const char *hs_error_string(int code);

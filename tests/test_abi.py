@@ -99,3 +99,12 @@ def test_plain_c_caller(lib, tmp_path):
                               str(lay["total"])]
     assert out[1] == hs.hs_error_string(hs.HS_ERR_INVALID_ARG)
     assert out[2].split() == [str(hs.HS_ERR_INVALID_ARG), "0"]
+
+
+def test_host_side_argument_errors_need_no_device(lib):
+    """Calls whose arguments are refused return before any CUDA call, so they can be checked without a GPU."""
+    for call in (lambda: hs.hs_host_alloc(0), lambda: hs.hs_host_free(0),
+                 lambda: hs.hs_probe_launch(0, 0, 1, 1, 1, 0), lambda: hs.hs_pool_destroy(0)):
+        with pytest.raises(hs.HsError) as e:
+            call()
+        assert e.value.code == hs.HS_ERR_INVALID_ARG

@@ -40,3 +40,39 @@ def test_two_ranks_take_the_slowest_time():
     for rank, slow, rate in res:
         assert slow == pytest.approx(20.0)
         assert rate == pytest.approx(2 * 1000 / 0.020)
+
+
+def _stub_measure(args, env):
+    """Stands in for the GPU work of one replica: rank r takes 10 (r + 1) ms for 100 units."""
+    import bench
+
+    slow = bench.max_over_ranks(10.0 * (env.rank + 1), env.dist)
+    return {"n_gpus": env.world, "rank": env.rank, "local": env.local, "steps": args.steps,
+            "value": bench.aggregate_rate(env.world, 100, slow), "slow_ms": slow}
+
+
+def test_gpus_flag_spawns_one_replica_per_gpu(capfd, monkeypatch):
+    """`bench.py --gpus 2` with no launcher starts two replica processes (RANK = LOCAL_RANK = 0, 1) that meet
+    over gloo; rank 0 alone prints the line, with the slowest rank's time."""
+    import json
+
+    import bench
+
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    rc = bench.spawn_replicas(2, ["--gpus", "2", "--steps", "7", "--warmup", "3"], measure_fn=_stub_measure)
+    assert rc == 0
+    lines = [ln for ln in capfd.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["rank"] == 0 and line["local"] == 0 and line["steps"] == 7
+    assert line["slow_ms"] == pytest.approx(20.0)
+    assert line["value"] == pytest.approx(2 * 100 / 0.020)
+
+
+def test_gpus_flag_must_match_the_launcher(monkeypatch):
+    import bench
+
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--gpus", "1"])
+    assert bench.parse_args(["--gpus", "2"]).gpus == 2

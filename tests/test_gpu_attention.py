@@ -109,7 +109,9 @@ def test_decode_large_batch_one_pair_per_request():
     """Up to the number of four-CTA clusters the device holds at once, a request's keys are split in two and the
     halves merged (the batches above); a larger batch runs one CTA pair over all of a request's keys. Both agree
     with the oracle, and the slot-list and history reads stay bit-identical."""
-    w = _w("mla_wide", 52, requests=48, ctx=2048, topk=200, slots=800, steps=2)
+    split_max = hs.hs_debug_attention()  # defaults kept; the largest batch whose keys are split on this device
+    w = _w("mla_wide", 52, requests=split_max + 10, ctx=2048, topk=200, slots=800, steps=2)
+    assert w.requests > split_max  # so this launch runs one pair per request
     sel_all = wl.gen_selections(w)[:, 0]
     rng = np.random.default_rng(52)
     buf = make_pool(w, noio=True)
@@ -269,3 +271,42 @@ def test_decode_history_from_host_memory():
         ref_out, ref_lse = _oracle(w, host, q_bits, sel_all[s], SCALE)
         _check(out_a.cpu().numpy(), lse_a.cpu().numpy(), ref_out, ref_lse, vstats, f"host step {s}")
     assert hs.hs_get_error(buf.handle) == 0
+
+
+@pytest.mark.parametrize("split", [True, False])
+def test_wait_timeout_is_reported_and_the_pool_stays_usable(split):
+    """Failure detection without a GPU fault. With the test hook, the tensor-core issuer of every CTA waits on a
+    barrier that nothing completes, under a short wait limit: the wait runs out before anything is issued, every
+    role stops, the kernel frees its tensor memory and returns, and the pool's error word reads HS_DEVERR_TIMEOUT.
+    The context stays usable: with the defaults restored, the same call gives the normal, exact result. Both
+    launch shapes: keys split over two CTA pairs per request, and one pair per request."""
+    split_max = hs.hs_debug_attention()
+    B = 3 if split else split_max + 2
+    w = _w(f"mla_to_{int(split)}", 61 + int(split), requests=B, ctx=4096, topk=64, slots=256, steps=2)
+    sel = wl.gen_selections(w)[:, 0]
+    buf = make_pool(w, noio=True)
+    host = buf.host.numpy().reshape(w.requests, w.ctx, w.row_bytes)
+    q_bits = wl.gen_queries(w.requests, H, DQK, w.seed)
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda()
+    out_slots = torch.empty((B, w.topk), dtype=torch.int32, device="cuda")
+    topk = torch.from_numpy(sel[1]).cuda()
+    for s in range(2):
+        hs.hs_step_begin(buf.handle)
+        hs.hs_resolve(buf.handle, 0, B, torch.from_numpy(sel[s]).cuda(), w.topk, out_slots)
+    out = torch.zeros((B, H, DV), device="cuda")
+    lse = torch.zeros((B, H), device="cuda")
+    torch.cuda.synchronize()
+    hs.hs_debug_attention(64, True)
+    try:
+        hs.hs_mla_decode(buf.handle, 0, B, q, out_slots, w.topk, None, 0, SCALE, out, lse)
+        torch.cuda.synchronize()
+    finally:
+        hs.hs_debug_attention(0, False)
+    assert hs.hs_get_error(buf.handle, clear=True) == hs.HS_DEVERR_TIMEOUT
+    assert hs.hs_get_error(buf.handle) == 0
+    out_a, lse_a, out_b, lse_b = _run_pair(buf, q, out_slots, topk, w.topk, SCALE)
+    assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
+    ref_out, ref_lse = _oracle(w, host, q_bits, sel[1], SCALE)
+    _check(out_a.cpu().numpy(), lse_a.cpu().numpy(), ref_out, ref_lse, _value_stats(host), "after a timeout")
+    assert hs.hs_get_error(buf.handle) == 0
+    buf.close()

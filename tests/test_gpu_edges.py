@@ -160,6 +160,53 @@ def test_wide_stamp_range_multi_pass_victim_sort():
     buf.close()
 
 
+@pytest.mark.parametrize("shape", ["narrow", "wide", "few_old", "ties", "empties_late"])
+def test_victim_choice_on_arbitrary_stamp_distributions(shape):
+    """The victim choice against the oracle on stamp layouts a short replay rarely reaches: after a few ordinary
+    steps, the stamps of the occupied slots are rewritten (identically on both sides, every stamp <= the step) and
+    the next steps resolved. narrow: a few recent steps; wide: ages spread over 1000 steps, so stamp bins are
+    clamped while the victims lie in exact bins; few_old: fewer very old slots than misses, so the threshold falls
+    in the clamped bin and the full sort runs; ties: three distinct stamps; empties_late: empty slots remain at a
+    late step."""
+    rng = np.random.default_rng(sum(map(ord, shape)))
+    batch, ctx, slots, k, R = 4, 5000, 300, 64, 16
+    buf = _pool(1, batch, ctx, slots, k, R, seed=5)
+    ora = oracle.OraclePool(ctx, slots, R, 1, batch, track_rows=False)
+    prev, sels = None, []
+    n_fill = 2 if shape == "empties_late" else 8
+    for s in range(n_fill):
+        prev = _rand_sel(rng, batch, k, ctx, prev, keep=0.3)
+        sels.append(prev)
+    _run(buf, ora, sels)
+    step = 2000
+    occ = ora.slot_tok[0] >= 0
+    st = ora.slot_stamp[0].copy()
+    for b in range(batch):
+        n = int(occ[b].sum())
+        if shape == "narrow":
+            v = rng.integers(step - 6, step + 1, size=n)
+        elif shape == "wide":
+            v = rng.integers(step - 1000, step + 1, size=n)
+        elif shape == "few_old":
+            v = np.full(n, step - 1)
+            v[rng.choice(n, size=5, replace=False)] = rng.integers(1, 20, size=5)
+        elif shape == "ties":
+            v = rng.choice(np.array([step - 300, step - 7, step]), size=n)
+        else:
+            v = rng.integers(step - 2, step + 1, size=n)
+        st[b][occ[b]] = v
+    ora.slot_stamp[0][...] = st
+    buf.view("slot_stamp")[0].copy_(torch.from_numpy(st).cuda())
+    later = []
+    for s in range(4):
+        prev = _rand_sel(rng, batch, k, ctx, prev, keep=0.25 if shape == "few_old" else 0.5)
+        later.append(prev)
+    _run(buf, ora, later, set_step=step)
+    _check_rows(buf)
+    assert hs.hs_get_error(buf.handle) == 0
+    buf.close()
+
+
 def test_long_token_keys():
     # ctx = 2^23: token keys need three 8-bit passes, the top pass nearly empty
     rng = np.random.default_rng(13)
@@ -297,6 +344,36 @@ def test_probe_link_measures_and_rejects():
         hs.hs_probe_link(host.ptr, dev, 1 << 20, 0)  # no iteration
     torch.cuda.synchronize()
     host.close()
+
+
+def test_host_alloc_failure_is_reported_and_leaves_cuda_usable():
+    """A page-locked allocation the host cannot satisfy (1 PiB) comes back as HS_ERR_CUDA with a null pointer,
+    without a sticky error: a normal allocation and a device launch work right after."""
+    with pytest.raises(hs.HsError) as e:
+        hs.hs_host_alloc(1 << 50)
+    assert e.value.code == hs.HS_ERR_CUDA
+    host = hs.HostBuffer(1 << 20)
+    dev = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    zc, cp = hs.hs_probe_link(host.ptr, dev, 1 << 20, 1)
+    assert zc > 0 and cp > 0
+    torch.cuda.synchronize()
+    host.close()
+
+
+def test_probe_launch_runs_and_checks_its_arguments():
+    """The launch-floor probe enqueues the resolve's launch shape with an empty kernel: it touches no memory
+    (the pool's state is unchanged) and refuses the arguments a resolve refuses."""
+    buf = _pool(4, 8, 2000, 256, 64, 48)
+    before = buf.meta.clone()
+    for nl, batch in ((1, 8), (4, 3), (2, 1)):
+        hs.hs_probe_launch(buf.handle, 0, nl, batch, 64)
+    hs.hs_probe_launch(buf.handle, 0, 1, 0, 64)  # batch 0: no-op
+    torch.cuda.synchronize()
+    assert torch.equal(buf.meta, before)
+    for bad in ((0, 5, 8, 64), (-1, 1, 8, 64), (0, 1, 9, 64), (0, 1, 8, 65), (0, 0, 8, 64)):
+        with pytest.raises(hs.HsError):
+            hs.hs_probe_launch(buf.handle, *bad)
+    buf.close()
 
 
 def test_checkpoint_and_resume():
