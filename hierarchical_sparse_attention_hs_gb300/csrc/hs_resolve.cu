@@ -1,41 +1,45 @@
 // Fused per-layer selection resolution for a hierarchical KV cache, sm_103a.
 //
-// Method: "HiSparse: Scaling Sparse-Attention Decoding with Hierarchical KV Cache Management" (Abstract): a
-// fused CUDA kernel resolves each layer's selections -- hit detection, LRU replacement and host-to-device
-// fetches -- inside the decode CUDA graph; only the missing rows that hit the top-k are fetched ("HiSparse"
-// knowledge card, Timeline). The policy (stamps = decode step, oldest stamp first with ties to the lowest slot,
-// misses paired with victims in ascending token order, empties first) is stated in hs.h.
+// Method: "HiSparse: Scaling Sparse-Attention Decoding with Hierarchical KV Cache Management" (Abstract): for every
+// layer, one kernel inside the decode step's CUDA graph looks the layer's selections up in a fixed-size GPU cache,
+// replaces least recently used entries and fetches the missing rows from host memory; only missing rows that the
+// top-k selects are brought over ("HiSparse" knowledge card, Timeline). The policy (stamps = decode step, oldest
+// stamp first with ties to the lowest slot, misses paired with victims in ascending token order, empties first) is
+// stated in hs.h.
 //
-// One launch resolves one layer for `batch` request-layers. A request-layer is served by a thread-block
-// cluster of C CTAs (C = 1, 2, 4 or 8, chosen by the host so that enough SMs issue host-link loads while the
-// grid stays within one wave). Every CTA of the cluster computes the whole resolution redundantly from the same
-// inputs -- deterministic, so the CTAs agree without exchanging data; a cluster barrier separates the last
-// read of the shared metadata from the first write, and the writes and row copies are partitioned by CTA rank.
-// There is no spin-wait anywhere.
+// One launch resolves one layer for `batch` request-layers. A request-layer is served by a thread-block cluster of
+// C CTAs (C = 1, 2, 4 or 8, chosen by the host so that enough SMs issue host-link loads while the grid stays within
+// one wave). Every CTA reads the request-layer's selection, slot stamps and slot tokens and finds the hits and the
+// misses itself; the victim choice is split between the CTAs and its pieces are exchanged through distributed
+// shared memory (asynchronous remote stores counted by mbarrier transaction bytes); a cluster barrier separates
+// the last read of the shared metadata from the first write; metadata writes and row copies are split by CTA.
+// Every wait is bounded; bad input never traps (it sets the sticky error word).
 //
 // Per CTA (512 threads), in shared memory:
 //   1. the slot stamps and slot tokens start for shared memory as asynchronous copies while each warp loads its
-//      run of the selection row; clear the hit bitmap (and the token bitmap);
+//      run of the selection row; the bitmaps and bucket counts are cleared and the exchange barriers set up;
 //   2. each warp gathers tok2slot for its run of selection entries (random 4-byte reads, several in flight per
-//      thread); a hit sets its slot's bit in the hit bitmap, a miss its token's bit in the token bitmap (a bit
-//      found set already is a repeated token);
+//      thread); a hit sets its slot's bit in the hit bitmap, a repeated slot or token is an error;
 //   3. the misses in selection order, by ballots over the same runs (identical in every CTA of the cluster);
 //   4. two warp groups at once, each on its own named barrier:
 //      A (warps 0-7): at once the first wave of row loads from host memory into registers -- the link is busy
-//         while the resolution goes on -- then the rank of every miss among the misses by token: a running
-//         count over the token bitmap (contexts up to 2^18 units; longer ones radix-sort the misses by token);
-//      B (warps 8-15): the victims -- a stable LSD radix sort (8-bit digits, per-warp digit rows, ranks from
-//         ballots, so the order is exact and deterministic) of the slots not hit, keyed by stamp - min stamp
-//         (one pass while the stamps span fewer than 256 steps; the stamp range is read from shared memory);
-//         the first m are the victims in (stamp, slot) order;
-//   5. group A, after the cluster barrier, per owned selection entry: a hit is stamped; a miss of rank j takes
-//      victim j (the old token is unmapped, the new one mapped, the slot stamped); out_slots in input order;
+//         while the resolution goes on -- then the rank of every miss among the misses by token: a counting sort
+//         of the miss tokens on their top bits (at most 2048 buckets), then the few smaller tokens in the bucket;
+//      B (warps 8-15): the victims. CTA r of the cluster takes the r-th range of slots; one pass over it gives the
+//         candidates' stamp range and, from ballot bit planes, how many candidates have each stamp modulo 32. The
+//         rows of all CTAs are exchanged; when the candidates span at most 32 stamps these are exact per-stamp
+//         counts, and the bin holding position m - 1 splits the bins taken whole from the one taken in slot
+//         order. Each CTA scatters its range's victims, in (stamp, slot) order, into every CTA's victim list.
+//         Wider stamp spans sort all candidates instead (stable LSD radix sort, in every CTA);
+//   5. group A, after the cluster barrier, per owned selection entry (runs of 32 entries, round-robin over the
+//      cluster): a hit is stamped; a miss of rank j takes victim j (the old token is unmapped, the new one mapped,
+//      the slot stamped); out_slots in input order;
 //   6. rows: the row chunks are split between the cluster's CTAs in interleaved runs of blocks of
-//      32 x COPY_UNROLL chunks (a run covers a whole row when rows span several blocks);
-//      group B starts on this CTA's blocks past the first wave at once (no other CTA reads the hot buffer, so
-//      this needs no barrier), group A lands its first wave in the victims' slots after step 5 and joins;
-//      warps take blocks from a shared counter. Loads are 16-byte ld.global.cv (a host row always comes over
-//      the link, never from a stale L2 line), straight into the hot buffer.
+//      32 x COPY_UNROLL chunks (a run covers a whole row when rows span several blocks); group B starts on this
+//      CTA's blocks past the first wave at once (no other CTA reads the hot buffer, so this needs no barrier),
+//      group A lands its first wave in the victims' slots after step 5 and joins; warps take blocks from a shared
+//      counter. Loads are 16-byte ld.global.cv (a host row always comes over the link, never from a stale L2
+//      line), straight into the hot buffer.
 
 #include <cuda_runtime.h>
 

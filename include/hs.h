@@ -2,12 +2,12 @@
  * hs.h -- C ABI of the hierarchical KV cache resolver for top-k sparse-attention decoding (GB300, sm_103a).
  *
  * The method is the per-layer selection resolution of "HiSparse: Scaling Sparse-Attention Decoding with
- * Hierarchical KV Cache Management" (Abstract): each request keeps its full KV history in host memory and a
- * small fixed-size GPU cache; one fused CUDA kernel per layer resolves the layer's top-k selections -- hit
- * detection, LRU replacement and host-to-device fetches -- inside the decode CUDA graph; models that share
- * selections across layers prefetch the next layer exactly. The "HiSparse" knowledge card (Timeline) adds that
- * only the missing rows that hit the top-k are back-filled into the request's hot buffer, and the "Hybrid
- * HiSparse" card (Timeline) that the single-pass fused kernel is CUDA-graph capturable.
+ * Hierarchical KV Cache Management" (Abstract): every request keeps its whole KV history in host memory and a small
+ * GPU cache of fixed size; for each layer, one kernel inside the decode step's CUDA graph looks the layer's top-k
+ * selections up in that cache, makes room by least-recently-used replacement and fetches what is missing from host
+ * memory; where layers share one selection, the next layer is prefetched exactly. By the "HiSparse" knowledge card
+ * (Timeline) only missing rows that the top-k actually selects are brought over, and by the "Hybrid HiSparse" card
+ * (Timeline) the single-pass kernel can be captured in a CUDA graph.
  *
  * Cache instance. One request-layer (layer l, request b) owns `slots` hot rows of `row_bytes` bytes and three
  * int32 arrays in device memory: tok2slot[ctx] (slot holding token t, or -1), slot_tok[slots] (token in slot v,
@@ -131,6 +131,8 @@ int hs_get_meta_layout(const hs_pool_desc *desc, hs_meta_layout *out);
  * Validate the descriptor, bind the pool to the current device, and enqueue on `stream` the initialisation of
  * the metadata: every cache empty (tok2slot = slot_tok = -1, stamps 0), step 0, counters and error word 0.
  * *out receives the opaque handle (host memory owned by the library until hs_pool_destroy).
+ * Basis: the two tiers of the HiSparse paper (Abstract) -- the full KV history in host memory and a cache of fixed
+ * size on the GPU -- bound together with the per-request maps that the resolution keeps.
  */
 int hs_pool_create(const hs_pool_desc *desc, hs_stream_t stream, hs_pool **out);
 
@@ -138,7 +140,10 @@ int hs_pool_create(const hs_pool_desc *desc, hs_stream_t stream, hs_pool **out);
 int hs_pool_reset(hs_pool *pool, hs_stream_t stream);
 
 /* Enqueue "step += 1" on the device step counter; call once per decode step before that step's resolves.
- * Stamps are decode step numbers, so every layer resolved in one step stamps with the same value. */
+ * Stamps are decode step numbers, so every layer resolved in one step stamps with the same value. Basis: the
+ * paper's least-recently-used replacement (Abstract) read with the decode step as the unit of recency, which makes
+ * a prefetch and the resolve that follows it in the same step stamp alike; the increment is a kernel so that it
+ * sits inside the step's CUDA graph ("Hybrid HiSparse" knowledge card, Timeline: graph-capturable). */
 int hs_step_begin(hs_pool *pool, hs_stream_t stream);
 
 /*
@@ -202,7 +207,7 @@ int hs_gather_history(hs_pool *pool, int32_t layer, int32_t batch, const int32_t
 
 /*
  * Consumer: sparse MLA decode attention over the rows a resolve selected, on the tensor cores (the read that the
- * hot buffer exists for: "HiSparse" paper, Abstract, model outputs unchanged; the "Hybrid HiSparse" knowledge card
+ * hot buffer exists for: "HiSparse" paper, Abstract, the model's outputs do not change; the "Hybrid HiSparse" card
  * builds on Sparse MLA). Absorbed multi-head latent attention, one decode step: every row is 576 bf16 values (the
  * 512-value latent, then the 64-value rotary key), so the pool's row_bytes must be 1152 (else
  * HS_ERR_UNSUPPORTED). For request b < batch and head h < 128, over the valid entries i of its slot list:
@@ -245,14 +250,18 @@ int hs_mla_decode_history(hs_pool *pool, int32_t layer, int32_t batch, const voi
 int hs_debug_attention(uint32_t wait_limit, int32_t stall, int32_t *split_max_batch);
 
 /* Synchronise the device, then read the sticky device error word into *out (HS_DEVERR_* bits); clear it when
- * `clear` is non-zero. */
+ * `clear` is non-zero. Basis: the pages say nothing about bad selections; the reading taken here is that a kernel
+ * inside a decode graph must never trap, so a row it cannot resolve is rejected and reported here instead. */
 int hs_get_error(hs_pool *pool, int32_t *out, int32_t clear);
 
 /* Synchronise the device, then read layer `layer`'s counters: out[0..3] = hits, misses, evictions, bytes.
- * Every call counts: a resolve that follows a prefetch of the same selection adds its k lookups as hits. */
+ * Every call counts: a resolve that follows a prefetch of the same selection adds its k lookups as hits. Basis:
+ * the paper measures the cost of the method as the host-to-device traffic of misses (Abstract); these are the
+ * counts that traffic follows from. */
 int hs_get_counters(hs_pool *pool, int32_t layer, uint64_t out[4]);
 
-/* Release the opaque handle. Caller memory is untouched. */
+/* Release the opaque handle. Caller memory is untouched. Basis: as hs_pool_create; all memory stays the
+ * caller's, so the library only frees its own small host struct. */
 int hs_pool_destroy(hs_pool *pool);
 
 /* Page-locked, device-mapped, portable host allocation for a host pool (not for the hot path). */

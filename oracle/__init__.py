@@ -4,9 +4,10 @@ Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.
 library path (``hierarchical_sparse_attention_hs_gb300``) never does, and the two share no code.
 
 The arithmetic lives in ``hs_oracle.c`` (plain C, one request-layer at a time, library ``qsort`` for every ordering
-step). It follows the per-layer resolution of the HiSparse paper (Abstract: hit detection, LRU replacement and
-host-to-device fetches resolved per layer inside the decode step; "model outputs are unchanged" because only KV
-placement changes) under the fully specified policy: hits take the current decode step as stamp; victims are the
+step). It follows the per-layer resolution of the HiSparse paper (Abstract): each layer's selections are looked
+up in the GPU cache, least recently used entries make room, and the missing rows come from host memory, within the
+decode step; only where the KV rows sit changes, so the model computes the same outputs. The policy is fully
+specified: hits take the current decode step as stamp; victims are the
 non-selected slots with the oldest stamp, ties to the lowest slot index; misses go to victims in ascending token
 order; empty slots (stamp 0) are used first.
 

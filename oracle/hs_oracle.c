@@ -3,10 +3,11 @@
  * CPU-baseline leg of the benchmark may call it; the library path never does. It shares no code, header or
  * constant with the CUDA path.
  *
- * What it computes (HiSparse paper, Abstract: "a fused CUDA kernel resolves each layer's selections -- hit
- * detection, LRU replacement, and host-to-device fetches"; AI Summary: hit detection, eviction and data migration
- * in one pass; HiSparse knowledge card, Timeline: only the missing rows that hit the top-k are back-filled into
- * the request's hot buffer), for ONE request-layer cache instance and one call at decode step `step`:
+ * What it computes, for ONE request-layer cache instance and one call at decode step `step`: the per-layer
+ * resolution of "HiSparse: Scaling Sparse-Attention Decoding with Hierarchical KV Cache Management" (Abstract, and
+ * its AI Summary): every selected token is looked up in the GPU cache, the least recently used entries not
+ * selected now make room, and only the selected rows that are missing come over from host memory ("HiSparse"
+ * knowledge card, Timeline), written out as plain sequential steps:
  *
  *   0. Validation. A negative entry is padding. If any entry is >= ctx, or a non-negative token appears twice,
  *      the whole row is rejected: out_slots is -1 everywhere, no state changes, and an error bit is returned.
