@@ -55,7 +55,8 @@ FLUSH_BYTES = 256 << 20
 MLA_SCALE = 1.0 / math.sqrt(192.0)  # softmax scale of the attention consumer: 1/sqrt(128 + 64)
 HEADLINE = ("shared", {"prefetch": True})
 # (workload, mode) of the default run after the headline; modes of one workload are adjacent so its pool is reused
-DEFAULT_SET = [("shared", {"shared_call": True}), ("tiny", {}), ("dsa", {}), ("multilayer", {}), ("quest", {})]
+DEFAULT_SET = [("shared", {"prefetch": True, "prefetch_depth": 2}), ("shared", {"prefetch": True, "prefetch_depth": 4}),
+               ("shared", {"shared_call": True}), ("tiny", {}), ("dsa", {}), ("multilayer", {}), ("quest", {})]
 HIDING_WORK_MB = 64.0  # per-layer work stand-in of the prefetch-hiding measurement on the headline workload
 
 
@@ -67,6 +68,8 @@ def describe(w: wl.Workload) -> str:
 
 def mode_name(mode: dict) -> str:
     on = [k for k in ("prefetch", "shared_call", "full_offload", "work_only", "attention") if mode.get(k)]
+    if mode.get("prefetch") and mode.get("prefetch_depth", 1) != 1:
+        on[on.index("prefetch")] = f"prefetch_depth={mode['prefetch_depth']}"
     if mode.get("layer_work_mb"):
         on.append(f"layer_work_mb={mode['layer_work_mb']:g}")
     if mode.get("tiered_frac") is not None:
@@ -282,7 +285,8 @@ class StepGraphs:
         self.sel_of = sel_of or (lambda s, ls: res.sel[s][ls])
         self.out_of = out_of or (lambda l: res.out[l])
         self.stream = torch.cuda.Stream()
-        self.side = torch.cuda.Stream() if mode.get("prefetch") else None
+        self.depth = int(mode.get("prefetch_depth", 1)) if mode.get("prefetch") else 0
+        self.sides = [torch.cuda.Stream() for _ in range(self.depth)]
         self.shared_call = bool(mode.get("shared_call")) and w.shared_across_layers
         self.layer_work = bool(mode.get("layer_work_mb")) or bool(mode.get("work_only"))
         if mode.get("full_offload"):
@@ -358,20 +362,24 @@ class StepGraphs:
                 self._resolve(l, sel(self._lsel(l)), self.out_of(l), st)
                 self._layer_work(l)
             return
-        # exact layer-wise prefetch: once layer l starts on the main stream, layer l+1 is resolved on the side
-        # stream; layer l+1's own resolve waits for it and then only re-stamps and emits its slots
-        side = self.side
+        # exact layer-wise prefetch, D layers ahead on D side streams: when layer l starts on the main stream, layer
+        # l + D is resolved on side stream (l + D) % D (at layer 0, layers 1 .. D); layer l's own resolve waits for
+        # its prefetch and then only re-stamps and emits its slots. D = 1: prefetch(l+1) beside resolve(l).
+        D = self.depth
         done = [None] * w.layers
         for l in range(w.layers):
             if done[l] is not None:
                 st.wait_event(done[l])
-            if l + 1 < w.layers:
+            ahead = range(1, min(D, w.layers - 1) + 1) if l == 0 else ([l + D] if l + D < w.layers else [])
+            if ahead:
                 started = torch.cuda.Event()
                 started.record(st)
-                side.wait_event(started)
-                self._prefetch(l + 1, sel(self._lsel(l + 1)), side)
-                done[l + 1] = torch.cuda.Event()
-                done[l + 1].record(side)
+                for j in ahead:
+                    side = self.sides[j % D]
+                    side.wait_event(started)
+                    self._prefetch(j, sel(self._lsel(j)), side)
+                    done[j] = torch.cuda.Event()
+                    done[j].record(side)
             self._resolve(l, sel(self._lsel(l)), self.out_of(l), st)
             self._layer_work(l)
 
@@ -765,6 +773,7 @@ def measure(env: Env, res: Resources, mode: dict, K: int, W: int, legs: set, cpu
                       "layers share one host pool (host_layer_stride 0); every miss still crosses the link"),
     }
     out.update(step_stats(rows, w, max(link)))
+    out["step_ms"] = [round(r[1], 4) for r in rows]
     out["roofline"] = roofline_of(w, mode, env, K * w.layers, n_kernels, tot, kern_ms, link, res, rows)
     # run-to-run spread: two more passes of the same K steps (after the timed region)
     if "spread" in legs:
@@ -832,6 +841,7 @@ def prefetch_hiding(env: Env, res: Resources, K: int, W: int, work_mb: float) ->
     for key, mode in (("work_only", {"work_only": True, "layer_work_mb": work_mb}),
                       ("resolve_work", {"layer_work_mb": work_mb}),
                       ("prefetch_work", {"prefetch": True, "layer_work_mb": work_mb}),
+                      ("prefetch2_work", {"prefetch": True, "prefetch_depth": 2, "layer_work_mb": work_mb}),
                       ("shared_call_work", {"shared_call": True, "layer_work_mb": work_mb})):
         g = StepGraphs(res, res.pool, mode)
         g.run(W, timed=False)
@@ -847,6 +857,9 @@ def prefetch_hiding(env: Env, res: Resources, K: int, W: int, work_mb: float) ->
     out["exposed_with_prefetch_ms"] = exposed_pf
     out["exposed_with_shared_call_ms"] = exposed_sc
     out["hidden_by_prefetch_frac"] = 1.0 - exposed_pf / exposed if exposed > 0 else None
+    exposed_pf2 = out["prefetch2_work_steady_ms"] - out["work_only_steady_ms"]
+    out["exposed_with_prefetch2_ms"] = exposed_pf2
+    out["hidden_by_prefetch2_frac"] = 1.0 - exposed_pf2 / exposed if exposed > 0 else None
     out["hidden_by_shared_call_frac"] = 1.0 - exposed_sc / exposed if exposed > 0 else None
     return out
 
@@ -993,10 +1006,12 @@ def gpu_measure(args, env: Env) -> dict:
         others = [] if args.headline_only else DEFAULT_SET
     else:
         head_name = args.workload
-        head_mode = {"prefetch": args.prefetch, "shared_call": args.shared_call,
+        head_mode = {"prefetch": args.prefetch, "prefetch_depth": args.prefetch_depth if args.prefetch else 1,
+                     "shared_call": args.shared_call,
                      "layer_work_mb": args.layer_work_mb, "work_only": args.work_only,
                      "full_offload": args.full_offload, "tiered_frac": args.tiered_frac, "attention": args.attention}
-        head_mode = {k: v for k, v in head_mode.items() if v not in (None, False, 0.0)}
+        head_mode = {k: v for k, v in head_mode.items() if v not in (None, False, 0.0) and
+                     not (k == "prefetch_depth" and v == 1)}
         others = []
     alias = args.workload == "all" or args.alias_host
     cache = {}
@@ -1125,6 +1140,8 @@ def parse_args(argv=None):
                     help="comma-separated legs: floor, e2e, noio, cpu, spread, hiding, attention")
     ap.add_argument("--alias-host", action="store_true", help="all layers read one host pool")
     ap.add_argument("--prefetch", action="store_true", help="layer-wise prefetch on a second stream")
+    ap.add_argument("--prefetch-depth", type=int, default=1,
+                    help="with --prefetch: prefetch this many layers ahead, on as many side streams")
     ap.add_argument("--layer-work-mb", type=float, default=0.0,
                     help="per-layer work stand-in after each resolve: hs_gather + a copy of this many MB")
     ap.add_argument("--work-only", action="store_true",

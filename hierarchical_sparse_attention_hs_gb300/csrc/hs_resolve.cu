@@ -592,7 +592,10 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
       gmax = __reduce_max_sync(0xffffffffu, gmax);
       gnc = __reduce_add_sync(0xffffffffu, gnc);
       ncand = gnc;
-      if (m <= gnc && gmax - gmin <= 31 && !xfail) {
+      if (m <= gnc && gnc == H && gmax == gmin && !xfail) {
+        // no slot is hit and every slot has the same stamp (a cold start into empty caches): victim j is slot j
+        for (int j = g.tid(); j < m; j += g.size()) s_vic[j] = j;
+      } else if (m <= gnc && gmax - gmin <= 31 && !xfail) {
         // Stamp bin d = stamp - gmin < 32, lane d's counts in column (gmin + d) % 32. The bin totals and their
         // prefix give T, the bin holding position m - 1: bins below T are taken whole, bin T in slot order up to
         // m, at positions in (bin, segment, slot) order, which is (stamp, slot) order -- ties to the lowest slot.
@@ -919,10 +922,16 @@ int init_meta(hs_pool* p, cudaStream_t s) {
   return HS_OK;
 }
 
-int pick_cluster(const hs_pool* p, int batch) {
+#ifndef HS_PREFETCH_TARGET
+// CTAs a prefetch aims for. A prefetch runs beside the layer's own work: half the resolve's footprint leaves that
+// work its SMs while still keeping enough loads in flight for the link.
+#define HS_PREFETCH_TARGET 32
+#endif
+
+int pick_cluster(const hs_pool* p, int batch, bool prefetch) {
   // Enough CTAs to keep the host link (or HBM, in no-IO mode) busy -- the link saturates with a few dozen
   // SMs -- without spilling the grid into a second wave.
-  const int target = p->noio ? p->resident : 64;
+  const int target = p->noio ? p->resident : (prefetch ? HS_PREFETCH_TARGET : 64);
   int c = 1;
   while (c < p->max_cluster && batch * c < target && batch <= p->max_active[2 * c]) c <<= 1;
   return c;
@@ -953,7 +962,7 @@ int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk
   a.ctx = p->d.ctx;
   a.slots = p->d.slots;
   a.row_bytes = p->d.row_bytes;
-  a.cluster = pick_cluster(p, batch);
+  a.cluster = pick_cluster(p, batch, out == nullptr && !empty);
   a.nlayers = nlayers;
   a.resident = resident;
   a.resident_stride = resident_stride;

@@ -51,7 +51,8 @@ def compare_state(buf, ora: oracle.OraclePool, tag="") -> None:
 
 
 def replay(w: wl.Workload, steps: int | None = None, host_layers: int = 1, noio: bool = False,
-           prefetch: bool = False, graphs: bool = False, mid_check: bool = True, shared_call: bool = False):
+           prefetch: bool = False, graphs: bool = False, mid_check: bool = True, shared_call: bool = False,
+           depth: int = 0):
     """Run `steps` decode steps of workload w on the GPU and in the oracle; compare out_slots after every step
     and the whole state at the midpoint and at the end. Returns (buf, oracle pool)."""
     ns = w.steps if steps is None else steps
@@ -65,6 +66,7 @@ def replay(w: wl.Workload, steps: int | None = None, host_layers: int = 1, noio:
     torch.cuda.synchronize()
     s0 = torch.cuda.Stream()  # a non-default stream, so the same code can be captured into a graph
     s1 = torch.cuda.Stream() if prefetch else None
+    sides = [torch.cuda.Stream() for _ in range(depth)]
 
     def lsel(l):
         return 0 if w.shared_across_layers else l
@@ -79,6 +81,25 @@ def replay(w: wl.Workload, steps: int | None = None, host_layers: int = 1, noio:
             return
         if not prefetch:
             for l in range(L):
+                hs.hs_resolve(pool, l, B, topk_all[s, lsel(l)], k, out[l], s0)
+            return
+        if depth:
+            # layer-wise, `depth` layers ahead on `depth` side streams: when layer l starts on s0, layer l + depth
+            # is prefetched (at layer 0, layers 1 .. depth); layer l's resolve waits for its own prefetch
+            done = [None] * L
+            for l in range(L):
+                if done[l] is not None:
+                    s0.wait_event(done[l])
+                ahead = range(1, min(depth, L - 1) + 1) if l == 0 else ([l + depth] if l + depth < L else [])
+                if ahead:
+                    started = torch.cuda.Event()
+                    started.record(s0)
+                    for j in ahead:
+                        side = sides[j % depth]
+                        side.wait_event(started)
+                        hs.hs_prefetch(pool, j, B, topk_all[s, lsel(j)], k, side)
+                        done[j] = torch.cuda.Event()
+                        done[j].record(side)
                 hs.hs_resolve(pool, l, B, topk_all[s, lsel(l)], k, out[l], s0)
             return
         # layer-wise prefetch: layer l+1 is resolved ahead on s1 while layer l is resolved on s0

@@ -64,6 +64,16 @@ def test_shared_with_layerwise_prefetch_is_exact():
     buf.close()
 
 
+@pytest.mark.parametrize("depth", [1, 2, 3])
+def test_shared_layerwise_prefetch_depth_is_exact(depth):
+    # prefetch `depth` layers ahead on as many side streams, as the benchmark does, captured in graphs: the state
+    # equals per-layer resolves (the oracle's)
+    w = wl.WORKLOADS["shared"]
+    buf, _ = gh.replay(w, steps=5, prefetch=True, graphs=True, depth=depth)
+    gh.check_hot_rows(buf, layers=[0, 1, 2, 40, 77])
+    buf.close()
+
+
 def test_shared_prefetch_in_graph():
     w = wl.WORKLOADS["shared"]
     buf, _ = gh.replay(w, steps=4, prefetch=True, graphs=True)
