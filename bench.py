@@ -200,6 +200,8 @@ def captured_traffic(w: wl.Workload, cold_launches: int, steady_launches: int, n
     if cap is None:
         return None
     d = cap["dram_bytes_per_launch"]
+    if d.get("cold") is None:  # a capture of steady launches only stands for every launch of the pass
+        return d["steady"]
     n = cold_launches + steady_launches
     return (cold_launches * d["cold"] + steady_launches * d["steady"]) / n if n else None
 
@@ -727,7 +729,7 @@ def roofline_of(w, mode, env: Env, n_launch_layers: int, n_kernels: int, tot, ke
         "traffic": captured_traffic(w, sum(w.layers for r in rows if r[0] == 0),
                                     sum(w.layers for r in rows if r[0] != 0)),
         "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed ncu capture "
-                          "(profiles/), null unless taken on these kernel sources",
+                          "(profiles/) of this workload's steady launches, null unless taken on these kernel sources",
         "kernel": "hs_resolve_kernel",
         "kernel_ms_per_launch": kern_ms / n_kernels,
         "launches": n_kernels,
@@ -1029,6 +1031,7 @@ def gpu_measure(args, env: Env) -> dict:
             # first-touch address translation of host pages is not charged to the timed steps; it also measures
             # the link
             r.link = measure_link(hs, torch, r.buf.host.ptr, r.buf.host.nbytes // 16 * 16)
+            torch.cuda.empty_cache()  # the probe's staging buffer goes back to the device
             cache[key] = r
         return cache[key]
 

@@ -24,6 +24,15 @@ def test_attention_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     assert bench.captured_attention_traffic(w) is None  # taken on other sources
 
 
+def test_steady_only_capture_stands_for_every_launch(tmp_path, monkeypatch):
+    w = wl.WORKLOADS["dsa"]
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    cap = {"kernel_sources_sha16": bench.kernel_sources_sha16(), "dram_bytes_per_launch": {"cold": None, "steady": 77}}
+    _write(tmp_path, f"hs_resolve_kernel_{w.name}_noio_ncu.json", cap)
+    assert bench.captured_traffic(w, 1, 3, noio=True) == 77
+    assert bench.captured_traffic(w, 1, 3) is None  # the host-link form has no capture here
+
+
 def test_resolve_traffic_weights_cold_and_steady_launches(tmp_path, monkeypatch):
     w = wl.WORKLOADS["dsa"]
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
@@ -39,7 +48,8 @@ def test_committed_captures_name_their_sources():
     files only."""
     import os
 
-    for name in ("hs_resolve_kernel_dsa_ncu.json", "hs_mla_decode_kernel_mla_ncu.json"):
+    for name in ("hs_resolve_kernel_dsa_ncu.json", "hs_resolve_kernel_dsa_noio_ncu.json",
+                 "hs_mla_decode_kernel_mla_ncu.json"):
         cap = json.load(open(os.path.join(bench.ROOT, "profiles", name)))
         key = "kernel_sources_sha16" if name.startswith("hs_resolve") else "attention_sources_sha16"
         assert len(cap[key]) == 16 and int(cap[key], 16) >= 0
