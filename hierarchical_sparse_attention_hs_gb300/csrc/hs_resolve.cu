@@ -94,6 +94,7 @@ struct ResolveArgs {
   const int32_t* resident;
   int64_t resident_stride;
   int32_t nlayers;
+  int32_t groups;                // layer groups: cluster (b, g) handles request b for the g-th run of layers
   int64_t meta_layer_ctx;        // int32 elements between layers in tok2slot
   int64_t meta_layer_slots;      // int32 elements between layers in slot_tok / slot_stamp
   int64_t src_layer_bytes;       // bytes between layers in the row source
@@ -278,18 +279,25 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
 
   const int C = a.cluster;
   const int rank = blockIdx.x % C;
-  const int b = blockIdx.x / C;
+  // Clusters are (request b, layer group g); a group is a run of consecutive layers that share one selection, so
+  // they hold identical metadata: each group resolves from its own first layer and updates only its own layers.
+  const int nreq = (int)gridDim.x / (C * a.groups);
+  const int b = (int)(blockIdx.x / C) % nreq, grp = (int)(blockIdx.x / C) / nreq;
+  const int lgrp = (a.nlayers + a.groups - 1) / a.groups;
+  const int l0 = grp * lgrp;
+  const int nl = min(a.nlayers, l0 + lgrp) - l0;  // >= 1: the host makes at most nlayers groups
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = a.k, H = a.slots, ctx = a.ctx, R = a.row_bytes;
   const int32_t step = __ldcg(a.step);
-  int32_t* t2s = a.tok2slot + (size_t)b * ctx;
-  int32_t* s2t = a.slot_tok + (size_t)b * H;
-  int32_t* stp = a.slot_stamp + (size_t)b * H;
+  int32_t* t2s = a.tok2slot + (size_t)l0 * (size_t)a.meta_layer_ctx + (size_t)b * ctx;
+  int32_t* s2t = a.slot_tok + (size_t)l0 * (size_t)a.meta_layer_slots + (size_t)b * H;
+  int32_t* stp = a.slot_stamp + (size_t)l0 * (size_t)a.meta_layer_slots + (size_t)b * H;
+  unsigned long long* counters = a.counters + 4 * (size_t)l0;
   const int32_t* sel = a.topk + (size_t)b * k;
-  int32_t* out = a.out_slots ? a.out_slots + (size_t)b * k : nullptr;
-  const uint8_t* src = a.src + (size_t)b * (size_t)a.src_req_stride;
+  int32_t* out = (a.out_slots && grp == 0) ? a.out_slots + (size_t)b * k : nullptr;  // identical in every group
+  const uint8_t* src = a.src + (size_t)l0 * (size_t)a.src_layer_bytes + (size_t)b * (size_t)a.src_req_stride;
   const int32_t* res = a.resident ? a.resident + (size_t)b * (size_t)a.resident_stride : nullptr;
-  uint8_t* hot = a.hot + (size_t)b * (size_t)H * (size_t)R;
+  uint8_t* hot = a.hot + (size_t)l0 * (size_t)a.hot_layer_bytes + (size_t)b * (size_t)H * (size_t)R;
   const int hwords = (H + 31) >> 5;
   const int cwords = (ctx + 31) >> 5;
   const int cpr = R >> 4;
@@ -683,7 +691,6 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
 
   // this CTA's row blocks past the first wave, one per warp at a time from a shared counter; with several
   // layers, local block n is block n % my_blocks of layer n / my_blocks
-  const int nl = a.nlayers;
   auto copy_rows = [&]() {
     while (true) {
       int n = 0;
@@ -758,14 +765,14 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   // counters
   nevict = __reduce_add_sync(0xffffffffu, nevict);
   if (lane == 0 && nevict)
-    for (int l = 0; l < nl; ++l) atomicAdd(a.counters + 4 * l + 2, (unsigned long long)nevict);
+    for (int l = 0; l < nl; ++l) atomicAdd(counters + 4 * l + 2, (unsigned long long)nevict);
   if (rank == 0 && tid == 0) {
     int nv = 0;
     for (int w = 0; w < NW; ++w) nv += s_wval[w];
     for (int l = 0; l < nl; ++l) {
-      atomicAdd(a.counters + 4 * l + 0, (unsigned long long)(nv - m));
-      atomicAdd(a.counters + 4 * l + 1, (unsigned long long)m);
-      atomicAdd(a.counters + 4 * l + 3, (unsigned long long)m * (unsigned long long)R);
+      atomicAdd(counters + 4 * l + 0, (unsigned long long)(nv - m));
+      atomicAdd(counters + 4 * l + 1, (unsigned long long)m);
+      atomicAdd(counters + 4 * l + 3, (unsigned long long)m * (unsigned long long)R);
     }
   }
 }
@@ -964,6 +971,27 @@ int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk
   a.row_bytes = p->d.row_bytes;
   a.cluster = pick_cluster(p, batch, out == nullptr && !empty);
   a.nlayers = nlayers;
+  a.groups = 1;
+  if (nlayers > 1) {
+    // Several layers sharing one selection: the layers are split into groups, one cluster per (request, group),
+    // as many groups as the device holds clusters of that size at once, so that the row copies of all the layers
+    // use the whole device. The cluster size is the largest whose grid reaches 80 % of the largest such grid
+    // (bigger clusters split the victim choice finer).
+    auto groups_for = [&](int c) {
+      const int fit = c > 1 ? p->max_active[c] : p->resident;
+      return fit >= batch ? std::min(nlayers, fit / batch) : 0;
+    };
+    int most = 0;
+    for (int c = 1; c <= p->max_cluster; c <<= 1) most = std::max(most, batch * c * groups_for(c));
+    for (int c = p->max_cluster; c >= 1; c >>= 1) {
+      const int g = groups_for(c);
+      if (g > 0 && 5 * batch * c * g >= 4 * most) {
+        a.cluster = c;
+        a.groups = g;
+        break;
+      }
+    }
+  }
   a.resident = resident;
   a.resident_stride = resident_stride;
   a.meta_layer_ctx = (int64_t)p->d.max_batch * p->d.ctx;
@@ -973,7 +1001,7 @@ int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3((unsigned)(batch * a.cluster), 1, 1);
+  cfg.gridDim = dim3((unsigned)(batch * a.cluster * a.groups), 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = smem_layout(k, p->d.slots, p->d.ctx).total;
   cfg.stream = s;
