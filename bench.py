@@ -14,8 +14,9 @@ hs_resolve(l). The other workloads, and the shared one with a single hs_resolve_
 ``per_workload`` with the same fields. ``--workload NAME`` measures one workload.
 
 Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the launching stream with a 256 MiB L2
-flush between steps (outside the events), barrier + synchronize around the whole region, max over ranks. Clocks
-are sampled with nvidia-smi during the timed regions.
+flush between steps (outside the events), barrier + synchronize around the whole region, max over ranks. A GPU-side
+spin of about 5 ms precedes each timed pass (outside the events) so that every step is enqueued before the GPU
+reaches it. Clocks are sampled with nvidia-smi during the timed regions.
 
 Roofline (the slower of two terms): miss-row bytes over the measured host link, and metadata + hot-buffer bytes
 over HBM (measured copy peak). The resolve kernels' duration is bounded by the step graph's, which is used.
@@ -58,6 +59,10 @@ HEADLINE = ("shared", {"prefetch": True})
 DEFAULT_SET = [("shared", {"prefetch": True, "prefetch_depth": 2}), ("shared", {"prefetch": True, "prefetch_depth": 4}),
                ("shared", {"shared_call": True}), ("tiny", {}), ("dsa", {}), ("multilayer", {}), ("quest", {})]
 HIDING_WORK_MB = 64.0  # per-layer work stand-in of the prefetch-hiding measurement on the headline workload
+# Before a timed pass the stream first runs a spin of this many GPU cycles (about 5 ms), outside the timed
+# intervals: the host then enqueues every step of the pass while the GPU is still busy, so a stall of the host
+# thread (the GPU machine is a shared VM) cannot fall between a step's start event and its graph launch.
+LEAD_CYCLES = 10_000_000
 
 
 def describe(w: wl.Workload) -> str:
@@ -352,7 +357,10 @@ class StepGraphs:
             for l in range(w.layers):
                 hs.hs_gather_history(self.pool, l, w.requests, sel(self._lsel(l)), w.topk, self.offload_buf, st)
             return
-        hs.hs_step_begin(self.pool, st)
+        if self.mode.get("prefetch"):
+            hs.hs_step_begin(self.pool, st)  # a prefetch on a side stream reads the step: its own launch
+        elif not self.floor:
+            hs.hs_step_begin_fused(self.pool)  # carried by the step's first resolve (no launch of its own)
         self._res_step = None if self.res.res is None else self.res.res[s % w.steps]
         if self.shared_call:
             self._shared(sel(0), self.out_of(0), st)
@@ -400,8 +408,10 @@ class StepGraphs:
         if self.mode.get("full_offload"):
             return w.layers
         if self.shared_call:
-            return 2 + w.layers * per_layer_work
-        return 1 + w.layers * (1 + per_layer_work) + (w.layers - 1 if self.mode.get("prefetch") else 0)
+            return 1 + w.layers * per_layer_work
+        if self.mode.get("prefetch"):
+            return 1 + w.layers * (1 + per_layer_work) + (w.layers - 1)
+        return w.layers * (1 + per_layer_work)
 
     def flush(self):
         with self.torch.cuda.stream(self.stream):
@@ -428,7 +438,13 @@ class StepGraphs:
                 rows.append((p, e0.elapsed_time(e1) if timed else 0.0, c))
             pending.clear()
 
+        def lead():
+            if timed:
+                with torch.cuda.stream(self.stream):
+                    torch.cuda._sleep(LEAD_CYCLES)
+
         self.reset()
+        lead()
         pos = 0
         for i in range(k_steps):
             if pos == len(self.graphs) or pos == self.w.steps:
@@ -436,6 +452,7 @@ class StepGraphs:
                 totals += self.res.counters()
                 pos = 0
                 self.reset()
+                lead()
             self.flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(self.stream):
@@ -794,7 +811,8 @@ def measure(env: Env, res: Resources, mode: dict, K: int, W: int, legs: set, cpu
         out["floor"] = {"ms_per_step": fms, "frac_of_step": fms / (total_ms / K),
                         "what": "the same step graph with every resolve replaced by an empty kernel launched with "
                                 "the resolve's configuration (hs_probe_launch): grid, cluster, shared memory, "
-                                "programmatic dependent launch; hs_step_begin kept"}
+                                "programmatic dependent launch; hs_step_begin kept where the step has it (prefetch "
+                                "pipelines), elsewhere the step increment rides on the first resolve"}
     if "e2e" in legs:
         nvtx.range_push("end to end")
         out["e2e"] = e2e_passes(res, mode, K, g)

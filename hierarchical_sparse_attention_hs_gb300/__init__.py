@@ -22,7 +22,7 @@ __all__ = [
     "hs_pool_destroy", "hs_host_alloc", "hs_host_free", "hs_error_string", "HS_DEVERR_RANGE", "HS_DEVERR_DUP",
     "HS_DEVERR_STATE", "HostBuffer", "PoolBuffers", "hs_probe_link", "hs_gather", "hs_gather_history",
     "hs_resolve_shared", "hs_resolve_tiered", "hs_mla_decode", "hs_mla_decode_history", "HS_DEVERR_TIMEOUT",
-    "MLA_HEADS", "MLA_D_QK", "MLA_D_V", "hs_probe_launch", "hs_debug_attention",
+    "MLA_HEADS", "MLA_D_QK", "MLA_D_V", "hs_probe_launch", "hs_debug_attention", "hs_step_begin_fused",
 ]
 
 HS_OK = 0
@@ -78,6 +78,7 @@ def load():
             "hs_pool_create": (ctypes.c_int, [P(hs_pool_desc), vp, P(vp)]),
             "hs_pool_reset": (ctypes.c_int, [vp, vp]),
             "hs_step_begin": (ctypes.c_int, [vp, vp]),
+            "hs_step_begin_fused": (ctypes.c_int, [vp]),
             "hs_resolve": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp]),
             "hs_prefetch": (ctypes.c_int, [vp, i32, i32, vp, i32, vp]),
             "hs_gather": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp]),
@@ -174,6 +175,10 @@ def hs_pool_reset(pool: int, stream=None) -> None:
 
 def hs_step_begin(pool: int, stream=None) -> None:
     _check(load().hs_step_begin(pool, _stream(stream)), "hs_step_begin")
+
+
+def hs_step_begin_fused(pool: int) -> None:
+    _check(load().hs_step_begin_fused(pool), "hs_step_begin_fused")
 
 
 def hs_resolve(pool: int, layer: int, batch: int, topk_idx, k: int, out_slots, stream=None) -> None:

@@ -18,6 +18,7 @@ struct hs_pool {
   const uint8_t* src;  // device-visible row source
   int32_t* step;
   int32_t* err;
+  int32_t begin_pending;  // step increments deferred to the next resolve-type launch (hs_step_begin_fused)
   unsigned long long* counters;
   int32_t* tok2slot;
   int32_t* slot_tok;

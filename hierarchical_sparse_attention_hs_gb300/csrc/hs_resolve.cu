@@ -82,6 +82,10 @@ struct ResolveArgs {
   unsigned long long* counters;  // layer's 4 counters
   const int32_t* step;
   int32_t* err;
+  // Fused step begin: this launch resolves at step + begin; the last of its CTAs to finish (counted in *done, which
+  // it leaves at 0) stores the advanced step for the launches after it. 0 for an ordinary call.
+  int32_t begin;
+  int32_t* done;
   const uint8_t* src;            // row source of this layer, request 0
   int64_t src_req_stride;
   uint8_t* hot;                  // layer base, [max_batch][slots][row_bytes]
@@ -288,7 +292,16 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   const int nl = min(a.nlayers, l0 + lgrp) - l0;  // >= 1: the host makes at most nlayers groups
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = a.k, H = a.slots, ctx = a.ctx, R = a.row_bytes;
-  const int32_t step = __ldcg(a.step);
+  const int32_t step = __ldcg(a.step) + a.begin;
+  // On every way out: the last CTA of a step-beginning launch publishes the advanced step. Only the reads of the
+  // old value must come first, and every thread of a CTA has read it (and used it) long before its thread 0 gets
+  // here, past several barriers; later launches read the new value once this grid has completed.
+  auto finish = [&]() {
+    if (a.begin && tid == 0 && atomicAdd(a.done, 1) == (int)gridDim.x - 1) {
+      *const_cast<int32_t*>(a.step) = step;
+      *a.done = 0;
+    }
+  };
   int32_t* t2s = a.tok2slot + (size_t)l0 * (size_t)a.meta_layer_ctx + (size_t)b * ctx;
   int32_t* s2t = a.slot_tok + (size_t)l0 * (size_t)a.meta_layer_slots + (size_t)b * H;
   int32_t* stp = a.slot_stamp + (size_t)l0 * (size_t)a.meta_layer_slots + (size_t)b * H;
@@ -678,6 +691,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
       for (int i = tid; i < k; i += NT)
         if (owned(i)) out[i] = -1;
     if (rank == 0 && tid == 0) atomicOr(a.err, (int)bad);
+    finish();
     return;
   }
 
@@ -775,6 +789,7 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
       atomicAdd(counters + 4 * l + 3, (unsigned long long)m * (unsigned long long)R);
     }
   }
+  finish();
 }
 
 // Gather rows by index, the read a sparse-attention kernel makes: row i of request b goes to
@@ -962,6 +977,12 @@ int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk
   a.counters = p->counters + 4 * (size_t)layer;
   a.step = p->step;
   a.err = p->err;
+  a.done = p->err + 1;  // the header's third word
+  a.begin = 0;
+  if (!empty && p->begin_pending) {
+    a.begin = p->begin_pending;
+    p->begin_pending = 0;
+  }
   a.src = p->src + (size_t)layer * (size_t)p->d.host_layer_stride;
   a.src_req_stride = p->d.host_req_stride ? p->d.host_req_stride : (int64_t)p->d.ctx * p->d.row_bytes;
   a.hot = static_cast<uint8_t*>(p->d.hot_buf) + rl0 * (size_t)p->d.slots * (size_t)p->d.row_bytes;
@@ -1088,6 +1109,7 @@ int hs_pool_create(const hs_pool_desc* desc, hs_stream_t stream, hs_pool** out) 
   if (!p) return HS_ERR_NO_MEMORY;
   p->d = *desc;
   p->lay = lay;
+  p->begin_pending = 0;
   p->device = dev;
   p->num_sms = sms;
   p->noio = desc->noio_src != nullptr;
@@ -1145,6 +1167,7 @@ int hs_pool_create(const hs_pool_desc* desc, hs_stream_t stream, hs_pool** out) 
 
 int hs_pool_reset(hs_pool* pool, hs_stream_t stream) {
   if (!pool) return HS_ERR_INVALID_ARG;
+  pool->begin_pending = 0;
   return init_meta(pool, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -1161,6 +1184,12 @@ int hs_step_begin(hs_pool* pool, hs_stream_t stream) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, hs_step_kernel, pool->step) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+int hs_step_begin_fused(hs_pool* pool) {
+  if (!pool) return HS_ERR_INVALID_ARG;
+  ++pool->begin_pending;
+  return HS_OK;
 }
 
 int hs_resolve(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* topk_idx, int32_t k,

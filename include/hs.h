@@ -109,7 +109,8 @@ typedef struct {
 } hs_pool_desc;
 
 /* Byte offsets of the arrays inside `meta` (for inspection and checkpointing; the layout is stable):
- *   step: int32; error: int32; counters: uint64 [layers][4] = (hits, misses, evictions, bytes fetched);
+ *   step: int32; error: int32 (the next int32 is the completion count of hs_step_begin_fused);
+ *   counters: uint64 [layers][4] = (hits, misses, evictions, bytes fetched);
  *   tok2slot: int32 [layers][max_batch][ctx]; slot_tok, slot_stamp: int32 [layers][max_batch][slots]. */
 typedef struct {
   size_t step;
@@ -145,6 +146,18 @@ int hs_pool_reset(hs_pool *pool, hs_stream_t stream);
  * a prefetch and the resolve that follows it in the same step stamp alike; the increment is a kernel so that it
  * sits inside the step's CUDA graph ("Hybrid HiSparse" knowledge card, Timeline: graph-capturable). */
 int hs_step_begin(hs_pool *pool, hs_stream_t stream);
+
+/*
+ * The same step increment without a launch of its own: it is carried by the next hs_resolve, hs_prefetch,
+ * hs_resolve_shared or hs_resolve_tiered call made on this pool from the host (in host call order, which is also
+ * the order in which a CUDA graph captures them). That call's kernel resolves at the advanced step and its last CTA
+ * stores the new step value, using the third 32-bit word of the metadata header as a completion count (left at 0),
+ * so a steady decode step of one layer is one launch. Valid only when no other call on the pool runs concurrently
+ * with that one (a prefetch on another stream, for instance, would read the step while it changes): pipelines
+ * with hs_prefetch keep hs_step_begin. Calls made twice add up; hs_pool_reset drops pending increments. Enqueues
+ * nothing; HS_ERR_INVALID_ARG for a null pool. Basis: as hs_step_begin.
+ */
+int hs_step_begin_fused(hs_pool *pool);
 
 /*
  * Resolve one layer's selections for requests 0..batch-1 (batch row b is pool request b) at the current step:

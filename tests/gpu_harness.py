@@ -52,7 +52,7 @@ def compare_state(buf, ora: oracle.OraclePool, tag="") -> None:
 
 def replay(w: wl.Workload, steps: int | None = None, host_layers: int = 1, noio: bool = False,
            prefetch: bool = False, graphs: bool = False, mid_check: bool = True, shared_call: bool = False,
-           depth: int = 0):
+           depth: int = 0, fused: bool = False):
     """Run `steps` decode steps of workload w on the GPU and in the oracle; compare out_slots after every step
     and the whole state at the midpoint and at the end. Returns (buf, oracle pool)."""
     ns = w.steps if steps is None else steps
@@ -72,7 +72,10 @@ def replay(w: wl.Workload, steps: int | None = None, host_layers: int = 1, noio:
         return 0 if w.shared_across_layers else l
 
     def enqueue(s):
-        hs.hs_step_begin(pool, s0)
+        if fused:
+            hs.hs_step_begin_fused(pool)  # carried by the first resolve below
+        else:
+            hs.hs_step_begin(pool, s0)
         if shared_call:
             # one call resolves every layer; all layers' out_slots are the same, written once
             hs.hs_resolve_shared(pool, 0, L, B, topk_all[s, 0], k, out[0], s0)

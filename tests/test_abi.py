@@ -104,7 +104,8 @@ def test_plain_c_caller(lib, tmp_path):
 def test_host_side_argument_errors_need_no_device(lib):
     """Calls whose arguments are refused return before any CUDA call, so they can be checked without a GPU."""
     for call in (lambda: hs.hs_host_alloc(0), lambda: hs.hs_host_free(0),
-                 lambda: hs.hs_probe_launch(0, 0, 1, 1, 1, 0), lambda: hs.hs_pool_destroy(0)):
+                 lambda: hs.hs_probe_launch(0, 0, 1, 1, 1, 0), lambda: hs.hs_pool_destroy(0),
+                 lambda: hs.hs_step_begin_fused(0)):
         with pytest.raises(hs.HsError) as e:
             call()
         assert e.value.code == hs.HS_ERR_INVALID_ARG

@@ -376,6 +376,34 @@ def test_probe_launch_runs_and_checks_its_arguments():
     buf.close()
 
 
+def test_fused_step_begins_add_up_and_reset_drops_them():
+    """Two fused begins before a resolve advance the step by two; a reset drops a pending one; a call that launches
+    nothing (batch 0) leaves it pending for the next."""
+    rng = np.random.default_rng(3)
+    buf = _pool(1, 2, 3000, 128, 32, 16)
+    ora = oracle.OraclePool(3000, 128, 16, 1, 2, track_rows=False)
+    out = torch.empty((2, 32), dtype=torch.int32, device="cuda")
+    sel = _rand_sel(rng, 2, 32, 3000)
+    hs.hs_step_begin_fused(buf.handle)
+    hs.hs_step_begin_fused(buf.handle)
+    hs.hs_resolve(buf.handle, 0, 0, torch.from_numpy(sel).cuda(), 32, out)  # batch 0: nothing launched
+    hs.hs_resolve(buf.handle, 0, 2, torch.from_numpy(sel).cuda(), 32, out)
+    ora.step_begin()
+    ora.step_begin()
+    expect = ora.resolve(0, sel, None)
+    torch.cuda.synchronize()
+    assert int(buf.view("step").item()) == 2
+    assert np.array_equal(out.cpu().numpy(), expect)
+    assert np.array_equal(buf.view("slot_stamp").cpu().numpy(), ora.slot_stamp)
+    hs.hs_step_begin_fused(buf.handle)
+    hs.hs_pool_reset(buf.handle)
+    hs.hs_resolve(buf.handle, 0, 2, torch.from_numpy(sel).cuda(), 32, out)
+    torch.cuda.synchronize()
+    assert int(buf.view("step").item()) == 0  # the reset dropped the pending begin
+    assert hs.hs_get_error(buf.handle) == 0
+    buf.close()
+
+
 def test_checkpoint_and_resume():
     """The pool's whole state is plain device arrays (metadata and hot buffer): copied out mid-sequence and copied
     back later, it makes the pool replay the same steps with the same outputs and state."""

@@ -88,3 +88,17 @@ def test_shared_selection_one_call_for_all_layers():
     buf, _ = gh.replay(w, steps=12, shared_call=True)
     gh.check_hot_rows(buf, layers=[0, 1, 40, 77])
     buf.close()
+
+
+@pytest.mark.parametrize("name,graphs,shared_call", [("dsa", False, False), ("dsa", True, False),
+                                                     ("multilayer", True, False), ("shared", True, True)])
+def test_fused_step_begin_is_exact(name, graphs, shared_call):
+    # the step increment carried by the first resolve of each step (no launch of its own): identical outputs and
+    # state, and the step counter advances once per step
+    w = wl.WORKLOADS[name]
+    steps = 10 if name != "multilayer" else 6
+    buf, ora = gh.replay(w, steps=steps, graphs=graphs, fused=True, shared_call=shared_call)
+    assert int(buf.view("step").item()) == steps == ora.step
+    assert int(buf.meta[8:12].view(torch.int32).item()) == 0  # the completion count is left at zero
+    gh.check_hot_rows(buf, layers=[0, w.layers - 1])
+    buf.close()
