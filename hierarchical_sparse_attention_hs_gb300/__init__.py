@@ -22,7 +22,7 @@ __all__ = [
     "hs_pool_destroy", "hs_host_alloc", "hs_host_free", "hs_error_string", "HS_DEVERR_RANGE", "HS_DEVERR_DUP",
     "HS_DEVERR_STATE", "HostBuffer", "PoolBuffers", "hs_probe_link", "hs_gather", "hs_gather_history",
     "hs_resolve_shared", "hs_resolve_tiered", "hs_mla_decode", "hs_mla_decode_history", "HS_DEVERR_TIMEOUT",
-    "MLA_HEADS", "MLA_D_QK", "MLA_D_V", "hs_probe_launch", "hs_debug_attention", "hs_step_begin_fused",
+    "MLA_HEADS", "MLA_D_QK", "MLA_D_V", "hs_probe_launch", "hs_debug_attention", "hs_step_begin_fused", "hs_probe_link_static", "HS_ERR_TOO_LARGE",
 ]
 
 HS_OK = 0
@@ -31,6 +31,7 @@ HS_ERR_CUDA = -2
 HS_ERR_NOT_MAPPED = -3
 HS_ERR_NO_MEMORY = -4
 HS_ERR_UNSUPPORTED = -5
+HS_ERR_TOO_LARGE = -6
 HS_DEVERR_RANGE = 1
 HS_DEVERR_DUP = 2
 HS_DEVERR_STATE = 4
@@ -96,6 +97,7 @@ def load():
             "hs_error_string": (ctypes.c_char_p, [ctypes.c_int]),
             "hs_probe_link": (ctypes.c_int, [vp, vp, sz, i32, vp, P(ctypes.c_double), P(ctypes.c_double)]),
             "hs_probe_launch": (ctypes.c_int, [vp, i32, i32, i32, i32, vp]),
+            "hs_probe_link_static": (ctypes.c_int, [vp, sz, i32, vp, P(ctypes.c_double), P(ctypes.c_double)]),
             "hs_debug_attention": (ctypes.c_int, [ctypes.c_uint32, i32, P(i32)]),
         }
         for name, (res, args) in sig.items():
@@ -134,6 +136,15 @@ def hs_probe_link(host_ptr: int, dev, nbytes: int, iters: int = 5, stream=None) 
     zc, cp = ctypes.c_double(), ctypes.c_double()
     _check(load().hs_probe_link(host_ptr, _addr(dev), nbytes, iters, _stream(stream), ctypes.byref(zc),
                                 ctypes.byref(cp)), "hs_probe_link")
+    return zc.value, cp.value
+
+
+def hs_probe_link_static(host_ptr: int, nbytes: int, iters: int = 5, stream=None) -> tuple:
+    """(zero-copy SM read GB/s, cudaMemcpyAsync H2D GB/s) with the library's own fixed device scratch (at most
+    16 MiB); for callers that have no device allocator."""
+    zc, cp = ctypes.c_double(), ctypes.c_double()
+    _check(load().hs_probe_link_static(host_ptr, nbytes, iters, _stream(stream), ctypes.byref(zc), ctypes.byref(cp)),
+           "hs_probe_link_static")
     return zc.value, cp.value
 
 

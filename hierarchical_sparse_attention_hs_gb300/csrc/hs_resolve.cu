@@ -47,6 +47,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "../../include/hs.h"
@@ -1364,8 +1365,95 @@ const char* hs_error_string(int code) {
     case HS_ERR_NOT_MAPPED: return "host pool is not page-locked device-mapped memory";
     case HS_ERR_NO_MEMORY: return "out of host memory";
     case HS_ERR_UNSUPPORTED: return "geometry needs more shared memory than the device offers";
+    case HS_ERR_TOO_LARGE: return "request larger than the fixed device scratch of hs_probe_link_static (16 MiB)";
     default: return "unknown error";
   }
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------------------------------
+// Link probe that allocates nothing (hs_probe_link_static)
+// ------------------------------------------------------------------------------------------------------------------
+
+// Its device scratch: the copy's destination and the read kernel's sink (the first HS_STATIC_PROBE_MAX bytes), then
+// four clock stamps. A module global, so every device that loads this library holds it until the process exits.
+constexpr size_t HS_STATIC_PROBE_MAX = (size_t)16 << 20;
+static __device__ __align__(256) unsigned char hs_static_probe_scratch[HS_STATIC_PROBE_MAX + 256];
+
+namespace {
+
+__global__ void hs_clock_stamp_kernel(unsigned long long* dst) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  *dst = t;
+}
+
+// Device address of the scratch on the current device, looked up once per device (a host-side name of a
+// __device__ array is not a device address).
+std::mutex g_static_probe_mu;
+void* g_static_probe_addr[64];
+
+int static_probe_scratch(unsigned char** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_static_probe_mu);
+  if (!g_static_probe_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, hs_static_probe_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return HS_ERR_CUDA;
+    }
+    g_static_probe_addr[dev] = p;
+  }
+  *out = static_cast<unsigned char*>(g_static_probe_addr[dev]);
+  return HS_OK;
+}
+
+}  // namespace
+
+extern "C" int hs_probe_link_static(const void* host, size_t bytes, int32_t iters, hs_stream_t stream,
+                                    double* zero_copy_gbs, double* memcpy_gbs) {
+  if (!host || bytes < 16 || (bytes & 15) || iters < 1 || !zero_copy_gbs || !memcpy_gbs ||
+      (reinterpret_cast<uintptr_t>(host) & 15))
+    return HS_ERR_INVALID_ARG;
+  if (bytes > HS_STATIC_PROBE_MAX) return HS_ERR_TOO_LARGE;
+  const void* dhost = mapped_host_ptr(host);
+  if (!dhost) return HS_ERR_NOT_MAPPED;
+  unsigned char* scratch = nullptr;
+  int rc = static_probe_scratch(&scratch);
+  if (rc != HS_OK) return rc;
+  unsigned long long* stamps = reinterpret_cast<unsigned long long*>(scratch + HS_STATIC_PROBE_MAX);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int dev_id = 0, sms = 0;
+  if (cudaGetDevice(&dev_id) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev_id) != cudaSuccess)
+    return HS_ERR_CUDA;
+  // The same two transfers as hs_probe_link, timed by device clock stamps written into the scratch (no events).
+  unsigned long long best_zc = ~0ull, best_cp = ~0ull;
+  for (int r = 0; r <= iters; ++r) {  // round 0 warms up
+    hs_clock_stamp_kernel<<<1, 1, 0, s>>>(stamps + 0);
+    hs_probe_read_kernel<<<2 * sms, 512, 0, s>>>(static_cast<const uint8_t*>(dhost), bytes >> 4,
+                                                  reinterpret_cast<unsigned*>(scratch));
+    hs_clock_stamp_kernel<<<1, 1, 0, s>>>(stamps + 1);
+    hs_clock_stamp_kernel<<<1, 1, 0, s>>>(stamps + 2);
+    if (cudaGetLastError() != cudaSuccess ||
+        cudaMemcpyAsync(scratch, host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return HS_ERR_CUDA;
+    hs_clock_stamp_kernel<<<1, 1, 0, s>>>(stamps + 3);
+    unsigned long long t[4];
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemcpy(t, stamps, sizeof(t), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return HS_ERR_CUDA;
+    if (r) {
+      best_zc = std::min(best_zc, t[1] - t[0]);
+      best_cp = std::min(best_cp, t[3] - t[2]);
+    }
+  }
+  *zero_copy_gbs = (double)bytes / (double)std::max(best_zc, 1ull);  // bytes per ns = GB/s
+  *memcpy_gbs = (double)bytes / (double)std::max(best_cp, 1ull);
+  return HS_OK;
+}

@@ -67,6 +67,7 @@ typedef struct hs_pool hs_pool;
 #define HS_ERR_NOT_MAPPED (-3)  /* host_pool is not page-locked, device-mapped memory */
 #define HS_ERR_NO_MEMORY (-4)   /* host struct allocation failed */
 #define HS_ERR_UNSUPPORTED (-5) /* geometry needs more shared memory per block than the device offers */
+#define HS_ERR_TOO_LARGE (-6)   /* request larger than the fixed device scratch of hs_probe_link_static */
 
 /* Bits of the sticky device error word. */
 #define HS_DEVERR_RANGE 1 /* a selected token was >= ctx */
@@ -298,6 +299,24 @@ int hs_probe_link(const void *host, void *dev, size_t bytes, int32_t iters, hs_s
  * launching alone puts under the step. Argument checks as hs_resolve_shared; touches no memory; capturable.
  */
 int hs_probe_launch(hs_pool *pool, int32_t layer, int32_t nlayers, int32_t batch, int32_t k, hs_stream_t stream);
+
+/*
+ * The link probe for callers that cannot allocate device memory. hs_probe_link needs a device buffer of `bytes`
+ * that serves only as scratch (the copy's destination, the read kernel's sink). A caller that links this library
+ * without a device allocator of its own -- plain C code that has only the page-locked host memory of hs_host_alloc,
+ * or a component whose framework hands out no scratch -- cannot provide it. This entry point allocates nothing:
+ * its scratch is a fixed 16 MiB array in the library's device module (plus 256 bytes of clock stamps), which every
+ * GPU that loads the library holds until the process exits. The paper has no counterpart; it is plumbing.
+ *   host: mapped page-locked host memory as for hs_probe_link; bytes: a multiple of 16, 16 .. 16 MiB, else
+ *   HS_ERR_TOO_LARGE (nothing is launched); iters >= 1. Same measurement as hs_probe_link (best of `iters` after one
+ *   warm-up, GB/s = 1e9 bytes/s), timed by device clock stamps instead of events.
+ * The first call on a device looks up the scratch's device address (cudaGetSymbolAddress) and keeps it; that call
+ * synchronises, like every call. Every call shares the one scratch array, which keeps whatever the last call left
+ * there (nothing in it has to start at zero): calls that overlap on the GPU -- two streams, or two host threads --
+ * race on it.
+ */
+int hs_probe_link_static(const void *host, size_t bytes, int32_t iters, hs_stream_t stream, double *zero_copy_gbs,
+                         double *memcpy_gbs);
 
 /* Static text for an HS_ERR_* code. */
 const char *hs_error_string(int code);
