@@ -57,7 +57,8 @@ MLA_SCALE = 1.0 / math.sqrt(192.0)  # softmax scale of the attention consumer: 1
 HEADLINE = ("shared", {"prefetch": True})
 # (workload, mode) of the default run after the headline; modes of one workload are adjacent so its pool is reused
 DEFAULT_SET = [("shared", {"prefetch": True, "prefetch_depth": 2}), ("shared", {"prefetch": True, "prefetch_depth": 4}),
-               ("shared", {"shared_call": True}), ("tiny", {}), ("dsa", {}), ("multilayer", {}), ("quest", {})]
+               ("shared", {"shared_call": True}), ("shared", {"full_offload": True}), ("tiny", {}), ("dsa", {}),
+               ("dsa", {"full_offload": True}), ("multilayer", {}), ("quest", {})]
 HIDING_WORK_MB = 64.0  # per-layer work stand-in of the prefetch-hiding measurement on the headline workload
 # Before a timed pass the stream first runs a spin of this many GPU cycles (about 5 ms), outside the timed
 # intervals: the host then enqueues every step of the pass while the GPU is still busy, so a stall of the host
@@ -843,7 +844,7 @@ def measure(env: Env, res: Resources, mode: dict, K: int, W: int, legs: set, cpu
             t_hbm = rf["frac"] * (nk_ms / K)
             noio["roofline"]["frac_above_floor"] = t_hbm / max(1e-9, nk_ms / K - fms)
         out["noio"] = noio
-    if "cpu" in legs and env.rank == 0:
+    if "cpu" in legs and env.rank == 0 and not (mode.get("full_offload") or mode.get("work_only")):
         host = res.host_rows_layer0()
         tiered = mode.get("tiered_frac")
         out["cpu_baseline"] = cpu_baseline(w, budget_s=cpu_budget, tiered_frac=tiered, host=host)
