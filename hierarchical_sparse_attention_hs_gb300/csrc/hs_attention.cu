@@ -24,23 +24,26 @@
 // barrier merges its own heads with what the other pair left. A pair's time is a chain of dependent steps per key
 // block, not a bandwidth, so two pairs per request halve it.
 // Warp roles per CTA:
-//   warps 0-3   softmax: thread h owns head h, which is TMEM lane h of the score and output accumulators;
-//   warp 4      lane 0 issues every tcgen05.mma (and warp 4 allocates / frees the tensor memory);
-//   warps 5-12  load the CTA's columns of the selected rows into shared memory with cp.async (zero rows for
-//               padding), 32 rows per block, two warps per key stage, prefetching each stage's next rows into L2;
-//   warp 13     hands the score-exchange buffers back to the peer once they have been read.
-// Shared memory: this CTA's columns of Q (128 x 256 or 320), four key stages (32 rows each), one P buffer and two
-// exchange buffers, in the no-swizzle interleaved layout: element (row r, column c) at (r/8)*G + (c/8)*128 +
+//   warps 0-7   softmax: warp w owns heads 32 (w % 4) .. +31 (TMEM lanes of its quarter) for the keys of its half
+//               w / 4 of every 64-key block; the two threads of a head agree on the block maximum through shared
+//               memory and an mbarrier, and each sums its own weights;
+//   warp 8      lane 0 issues every tcgen05.mma (and warp 8 allocates / frees the tensor memory);
+//   warps 9-12  load the CTA's columns of the selected rows into shared memory with cp.async (zero rows for
+//               padding), 64 rows per block, two warps per key stage (one per half of the block's keys),
+//               prefetching each stage's next rows into L2;
+//   warp 13     hands the score-exchange buffer back to the peer once it has been read.
+// Shared memory: this CTA's columns of Q (128 x 256 or 320), two key stages (64 rows each), one P buffer and one
+// exchange buffer, in the no-swizzle interleaved layout: element (row r, column c) at (r/8)*G + (c/8)*128 +
 // (r%8)*16 + (c%8)*2, where G is the byte size of an 8-row group (one spare 128-byte slot included). A key stage
 // serves the score GEMM as a K-major operand (rows = keys) and the value GEMM as an MN-major operand (the same
 // bytes read with the two strides exchanged).
-// Tensor memory (512 columns): two 32-column score buffers, and the 256-column output half at column 256.
-// Per key block j: partial S = Q K^T (16 or 20 MMAs of 128x32x16) into score buffer j%2; the softmax threads
+// Tensor memory (512 columns): two 64-column score buffers, and the 256-column output half at column 256.
+// Per key block j: partial S = Q K^T (16 or 20 MMAs of 128x64x16) into score buffer j%2; the softmax threads
 // read it, store it into the peer's exchange buffer with st.async (completing the bytes the peer's barrier
 // expects), wait for the peer's part, and update the running max m (raised only when a block's maximum exceeds
 // it by more than 8 in log2 units, which bounds P and O by 2^8 and makes the rescale of O rare); they write
 // P = 2^(s - m) rounded to bf16 into the P buffer once the value GEMM of block j-1 has read it, and sum the
-// rounded values; then O += P V (two 128x256x16 MMAs). The score GEMM of block j+1 overlaps the softmax of
+// rounded values; then O += P V (four 128x256x16 MMAs). The score GEMM of block j+1 overlaps the softmax of
 // block j. The output leaves through a shared tile in whole 128-byte row segments. mbarriers order the roles,
 // within the CTA and across the pair; every wait is bounded: on running out
 // it sets an abort flag that ends every role and the HS_DEVERR_TIMEOUT bit of the pool's error word, after the
@@ -64,9 +67,10 @@ constexpr int DQK = 576;
 constexpr int DV = 512;
 constexpr int DV_HALF = DV / 2;
 constexpr int ROW_BYTES = DQK * 2;
-constexpr int KB = 32;     // keys per block (the N of the score GEMM)
-constexpr int NSTAGE = 4;  // key stages
-constexpr int NPB = 1;     // P buffers
+constexpr int KB = 64;       // keys per block (the N of the score GEMM)
+constexpr int KH = KB / 2;   // keys of a block per softmax thread (two threads per head)
+constexpr int NSTAGE = 4;    // key stages
+constexpr int NPB = 1;       // P buffers
 // Score-GEMM columns of each CTA of a request's pair: CTA 0 the first DSPLIT (its value half), CTA 1 the rest,
 // which contain its value half (columns 256..511).
 constexpr int DSPLIT = 256;
@@ -74,36 +78,40 @@ constexpr int MAX_NDIM = DQK - DSPLIT;
 // An 8-row group of a CTA's columns holds its 16-byte chunks at 128-byte spacing plus one spare 128-byte slot, so
 // that successive groups do not start at power-of-two distances.
 constexpr int MAX_GROUP = (MAX_NDIM / 8 + 1) * 128;
-constexpr int Q_BYTES = (HEADS / 8) * MAX_GROUP;
 constexpr int STAGE_BYTES = (KB / 8) * MAX_GROUP;
 constexpr int P_GROUP = (KB / 8) * 128;    // bytes of one 8-head group of P (128 x KB)
 constexpr int P_BYTES = HEADS * KB * 2;
 constexpr int X_BYTES = HEADS * KB * 4;    // the peer's partial scores of one block, fp32
-constexpr int SOFTMAX_WARPS = 4, MMA_WARP = 4, LOAD_WARP0 = 5;
-constexpr int STAGE_WARPS = 2;             // loader warps per key stage
+// Warp roles: softmax warps 0-7 (warp w: heads 32 (w % 4) .. +31, the block's keys KH (w / 4) .. +KH-1), the MMA
+// issuer, loader warps (two per key stage), the exchange warp.
+constexpr int SOFTMAX_WARPS = 8, SOFTMAX_THREADS = SOFTMAX_WARPS * 32, MMA_WARP = 8, LOAD_WARP0 = 9;
+constexpr int STAGE_WARPS = 2;             // loader warps per key stage (one per half of the block's keys)
 constexpr int LOAD_WARPS = NSTAGE * STAGE_WARPS;
-constexpr int XCHG_WARP = LOAD_WARP0 + LOAD_WARPS;  // hands exchange buffers back to the peer
+constexpr int XCHG_WARP = LOAD_WARP0 + LOAD_WARPS;  // hands the exchange buffer back to the peer
 constexpr int NTHREADS = (XCHG_WARP + 1) * 32;
-constexpr uint32_t TMEM_COLS = 512, TMEM_S = 0, TMEM_O = 256;
+// Tensor memory: this CTA's columns of Q (the score GEMM's A operand, two bf16 per 32-bit column: at most 160
+// columns), the score buffer (KB columns) and the output half (256 columns).
+constexpr uint32_t TMEM_COLS = 512, TMEM_Q = 0, TMEM_S = 192, TMEM_O = 256;
+static_assert(TMEM_Q + MAX_NDIM / 2 <= TMEM_S && TMEM_S + KB <= TMEM_O, "tensor memory columns");
 constexpr unsigned WAIT_LIMIT = 1u << 20;  // try_wait rounds (each may suspend briefly) before a wait gives up
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int OFF_K = 0;
 constexpr int OFF_P = OFF_K + NSTAGE * STAGE_BYTES;
-constexpr int OFF_X = OFF_P + NPB * P_BYTES;       // two exchange buffers
-constexpr int OFF_KEY = OFF_X + 2 * X_BYTES;       // row pointers of each stage: [NSTAGE][KB]
-// mbarriers: kfull[NSTAGE] kempty[NSTAGE] sfull[2] sempty[2] pfull[NPB] pdone[NPB] odone drain xfull[2] xempty[2]
-// xread[2] tdone
-constexpr int NBAR = 2 * NSTAGE + 4 + 2 * NPB + 2 + 6 + 1;
+constexpr int OFF_X = OFF_P + NPB * P_BYTES;       // one exchange buffer
+constexpr int OFF_KEY = OFF_X + X_BYTES;           // row pointers of each stage: [NSTAGE][KB]
+// mbarriers: kfull[NSTAGE] kempty[NSTAGE] sfull sempty pfull[NPB] pdone[NPB] odone drain xfull xempty xread tdone
+// pmx[4] (the two softmax warps of a head quarter agreeing on the block maximum) qready (Q is in tensor memory)
+constexpr int NBAR = 2 * NSTAGE + 2 + 2 * NPB + 2 + 3 + 1 + 4 + 1;
 constexpr int OFF_BAR = OFF_KEY + NSTAGE * KB * 8;
-// TMEM address, abort flag, per-stage stop flags, per-stage masks of the keys with a row
+// TMEM address, abort flag, per-stage stop flags, per-stage masks of the keys with a row (one word per half)
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr int OFF_PMAX = (OFF_MISC + 8 + 4 * NSTAGE + 8 * NSTAGE + 15) & ~15;  // [2 parities][2 halves][HEADS]
 // (m, l) per head from the CTA of the other key half, for the heads this CTA merges
-constexpr int OFF_COMB = (OFF_MISC + 8 + 8 * NSTAGE + 15) & ~15;
+constexpr int OFF_COMB = OFF_PMAX + 2 * 2 * HEADS * 4;
 constexpr int SMEM_BYTES = OFF_COMB + HEADS * 8;
 static_assert(SMEM_BYTES <= 232448, "shared memory per block");
-static_assert(4 * 32 * 36 * 4 <= NSTAGE * STAGE_BYTES, "output tiles of the four softmax warps fit the key stages");
-static_assert(KB == 32, "one loader lane per key of a block");
+static_assert(SOFTMAX_WARPS * 32 * 36 * 4 <= NSTAGE * STAGE_BYTES, "output tiles of the softmax warps fit the stages");
+static_assert(KB == 2 * 32 && STAGE_WARPS >= 2, "one lane of the stage's first two warps per key of a block");
 
 struct MlaArgs {
   const uint16_t* q;        // bf16 [batch][HEADS][DQK]
@@ -255,20 +263,30 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// The same with the A operand in tensor memory (M lanes; a 16-wide K chunk of bf16 is 8 columns).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
 // Score MMAs K0 .. K1-1 of a block (16 columns each, K1 - K0 even). The tensor pipe takes few instructions ahead,
 // so every instruction of the issuing loop shows up in the MMA rate: a loop with a run-time count and the
 // descriptor arithmetic per MMA ran at 46 ns per MMA, this one at about 31 (the rate of the MMA itself). Two MMAs
 // per iteration rather than the whole sequence unrolled: the fully unrolled issue code made the softmax warps of
 // some SMs twice as slow (instruction fetch), the same on every launch.
 template <int K0, int K1>
-__device__ __forceinline__ void issue_qk(uint32_t dst, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+__device__ __forceinline__ void issue_qk(uint32_t dst, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
   static_assert((K1 - K0) % 2 == 0, "two MMAs per iteration");
-  uint64_t a = a_desc + (uint64_t)(16 * K0), b = b_desc + (uint64_t)(16 * K0);
+  uint32_t a = a_tmem + 8u * K0;
+  uint64_t b = b_desc + (uint64_t)(16 * K0);
 #pragma unroll 1
   for (int kk = K0; kk < K1; kk += 2) {
-    mma_bf16(dst, a, b, idesc, kk != 0 ? 1u : 0u);
-    mma_bf16(dst, a + 16, b + 16, idesc, 1u);
-    a += 32;
+    mma_bf16_ta(dst, a, b, idesc, kk != 0 ? 1u : 0u);
+    mma_bf16_ta(dst, a + 8, b + 16, idesc, 1u);
+    a += 16;
     b += 32;
   }
 }
@@ -289,6 +307,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint4 (&v)[4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z), "r"(v[1].w),
+      "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y), "r"(v[3].z), "r"(v[3].w)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -303,16 +329,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Output half of one softmax warp's 32 heads: out[h][c] = w0 * O[h][c] (+ w1 * out[h][c], what the CTA of the
-// other key half left there, wherever that head's w1 != 0), O read from tensor memory (zero without it). Each
-// thread holds its head's row; 32-column slices go through a shared tile (rows 144 bytes apart: conflict-free
-// 16-byte accesses both ways) so that the global reads and writes are whole 128-byte row segments.
+// One softmax warp's part of the output: its 32 heads, columns c_lo .. c_lo + 127 of the CTA's value half:
+// out[h][c] = w0 * O[h][c] (+ w1 * out[h][c], what the CTA of the other key half left there, wherever that head's
+// w1 != 0), O read from tensor memory (zero without it). Each thread holds its head's row; 32-column slices go
+// through a shared tile (rows 144 bytes apart: conflict-free 16-byte accesses both ways) so that the global reads and
+// writes are whole 128-byte row segments.
 __device__ __forceinline__ void store_out_rows(uint32_t trow, bool have_o, float w0, float w1, float* tile,
-                                               float* rows, int lane) {
+                                               float* rows, int lane, int c_lo) {
   constexpr int TS = 36;  // tile row stride in floats
   const bool merge = __any_sync(0xffffffffu, w1 != 0.f);
   const int col4 = lane & 7;
-  for (int c0 = 0; c0 < DV_HALF; c0 += 32) {
+  for (int c0 = c_lo; c0 < c_lo + DV_HALF / 2; c0 += 32) {
     float o[32];
     if (have_o) {
       tmem_ld16(trow + TMEM_O + c0, *reinterpret_cast<float(*)[16]>(o));
@@ -375,70 +402,82 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   // this CTA's score-GEMM columns: [d0, d0 + 8 * nch)
   const int d0 = half ? DSPLIT : 0, nch = (half ? DQK - DSPLIT : DSPLIT) / 8, grp = (nch + 1) * 128;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t *kfull = bars, *kempty = bars + NSTAGE, *sfull = bars + 2 * NSTAGE, *sempty = sfull + 2,
-           *pfull = sempty + 2, *pdone = pfull + NPB, *odone = pdone + NPB, *drain = odone + 1, *xfull = drain + 1,
-           *xempty = xfull + 2, *xread = xempty + 2, *tdone = xread + 2;
+  uint64_t *kfull = bars, *kempty = bars + NSTAGE, *sfull = bars + 2 * NSTAGE, *sempty = sfull + 1,
+           *pfull = sempty + 1, *pdone = pfull + NPB, *odone = pdone + NPB, *drain = odone + 1, *xfull = drain + 1,
+           *xempty = xfull + 1, *xread = xempty + 1, *tdone = xread + 1, *pmx = tdone + 1, *qready = pmx + 4;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   volatile int* stage_stop = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
-  uint32_t* kmask = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 8 + 4 * NSTAGE);  // bit i: key i has a row
+  // [stage][half]: bit i = key half * 32 + i of the stage's block has a row
+  uint32_t* kmask = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 8 + 4 * NSTAGE);
+  float* pshare = reinterpret_cast<float*>(smem + OFF_PMAX);  // [parity][key half][head]: block maxima, normalisers
   const uint8_t** keyp = reinterpret_cast<const uint8_t**>(smem + OFF_KEY);
 
-  // this CTA's columns of Q: head h, columns d0 + 8c .. d0 + 8c + 7 at (h/8)*grp + c*128 + (h%8)*16; thread
-  // order walks that layout (8 heads of one chunk, then the next chunk), so a warp's copies fill consecutive
-  // 16-byte slots of shared memory
-  const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q + (size_t)b * HEADS * DQK) + d0 * 2;
-  for (int e = tid; e < HEADS * nch; e += NTHREADS) {
-    const int g = e / (8 * nch), rem = e - g * 8 * nch, c = rem >> 3, h = g * 8 + (rem & 7);
-    cp_async16(smem + OFF_Q + g * grp + c * 128 + (h & 7) * 16, qsrc + (size_t)h * ROW_BYTES + c * 16);
+  // softmax warps: head quarter q (tensor-memory lanes 32 q .. 32 q + 31), key half kh of every block; thread =
+  // head h
+  const int q = warp & 3, kh = (warp >> 2) & 1, h = q * 32 + lane;
+  // Q is the score GEMM's A operand in tensor memory: lane h holds head h's columns of this CTA, two per 32-bit
+  // column. The softmax thread (h, kh) loads half of them (nq 16-byte chunks) now and stores them once the tensor
+  // memory is allocated.
+  const int nq = nch / 2;
+  uint4 qv[MAX_NDIM / 16];
+  if (warp < SOFTMAX_WARPS) {
+    const uint4* qrow = reinterpret_cast<const uint4*>(a.q + ((size_t)b * HEADS + h) * DQK + d0) + kh * nq;
+#pragma unroll
+    for (int i = 0; i < MAX_NDIM / 16; ++i)
+      if (i < nq) qv[i] = __ldg(qrow + i);
   }
-  cp_async_commit();
 
   // Loaders: the STAGE_WARPS warps of stage s fill it with blocks s, s + NSTAGE, ... (this CTA's columns of each
-  // row). The stage's first warp looks up the block's 32 rows (lane i: key i) into the stage's row pointers, a
-  // named barrier hands them to the other warps, every thread copies its share of the 16-byte chunks, and the first
-  // warp starts the stage's next rows on their way into L2. Each stage's first block is started here, alongside
-  // Q, before anything waits, and lands before the barrier below; the L2 prefetches of those stages' next blocks
-  // wait until after it, so that they do not compete with the first copies.
+  // row). Warp lsub of the stage looks up keys lsub * 32 + lane of the block into the stage's row pointers and
+  // validity mask, a named barrier hands them to the other warp, every thread copies its share of the 16-byte
+  // chunks, and each warp starts its half of the stage's next rows on their way into L2. Each stage's first block
+  // is started here, alongside Q, before anything waits, and lands before the barrier below.
   const bool loader = warp >= LOAD_WARP0 && warp < XCHG_WARP;
   const int ls = (warp - LOAD_WARP0) / STAGE_WARPS, lsub = (warp - LOAD_WARP0) % STAGE_WARPS;
   uint8_t* const lst = smem + OFF_K + ls * STAGE_BYTES;
-  auto load_rows = [&](int j) {
-    if (lsub == 0) {
-      const int i = (jb + j) * KB + lane;
-      const uint8_t* r = i < k ? row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i)) : nullptr;
-      keyp[ls * KB + lane] = r;
+  // the row of this lane's key of block j (its slot-list entry read from global memory)
+  auto lookup = [&](int j) -> const uint8_t* {
+    const int i = (jb + j) * KB + lsub * 32 + lane;
+    return (lsub < 2 && i < k) ? row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i)) : nullptr;
+  };
+  // publish a block's rows to the stage (the stage must be free) and to the other warp of the stage
+  auto publish = [&](const uint8_t* r) {
+    if (lsub < 2) {
+      keyp[ls * KB + lsub * 32 + lane] = r;
       const uint32_t m = __ballot_sync(0xffffffffu, r != nullptr);
-      if (lane == 0) kmask[ls] = m;
+      if (lane == 0) kmask[ls * 2 + lsub] = m;
     }
     named_sync(1 + ls, STAGE_WARPS * 32);
   };
   auto prefetch_next = [&](int j) {
-    if (lsub == 0) {
-      // this CTA's part of the rows of the stage's next block starts for L2 while these copies land
-      const int i2 = (jb + j + NSTAGE) * KB + lane;
-      if (j + NSTAGE < nb && i2 < k) {
-        const uint8_t* r2 = row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i2));
-        if (r2) prefetch_l2(r2 + d0 * 2, (uint32_t)nch * 16u);
-      }
+    // this CTA's part of the rows of the stage's next block starts for L2 while these copies land
+    const int i2 = (jb + j + NSTAGE) * KB + lsub * 32 + lane;
+    if (lsub < 2 && j + NSTAGE < nb && i2 < k) {
+      const uint8_t* r2 = row_of(a, b, ld_fresh(a.idx + (size_t)b * k + i2));
+      if (r2) prefetch_l2(r2 + d0 * 2, (uint32_t)nch * 16u);
     }
   };
-  auto copy_rows = [&](int j) {
-    // thread order walks the shared-memory layout (8 rows of one chunk, then the next chunk), so a warp's copies
-    // fill consecutive 16-byte slots
-    for (int e = lsub * 32 + lane; e < KB * nch; e += STAGE_WARPS * 32) {
-      const int g = e / (8 * nch), rem = e - g * 8 * nch, c = rem >> 3, r = g * 8 + (rem & 7);
-      uint8_t* dst = lst + g * grp + c * 128 + (r & 7) * 16;
-      const uint8_t* src = keyp[ls * KB + r];
-      if (src)
-        cp_async16(dst, src + d0 * 2 + c * 16);
-      else
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+  auto copy_rows = [&](int) {
+    // lane = (row rr of an 8-row group, one of 4 consecutive chunks): a warp's copies fill 512 consecutive bytes
+    // of shared memory (the group's slots of 4 chunks), and the two warps of the stage take alternate 4-chunk runs
+    const int rr = lane & 7, c0 = lsub * 4 + (lane >> 3);
+#pragma unroll 1
+    for (int g = 0; g < KB / 8; ++g) {
+      const uint8_t* src = keyp[ls * KB + g * 8 + rr];
+      uint8_t* dst = lst + g * grp + rr * 16;
+      if (src) {
+        src += d0 * 2;
+        for (int c = c0; c < nch; c += 4 * STAGE_WARPS) cp_async16(dst + c * 128, src + c * 16);
+      } else {
+        for (int c = c0; c < nch; c += 4 * STAGE_WARPS)
+          *reinterpret_cast<uint4*>(dst + c * 128) = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
     cp_async_commit();
   };
   if (loader && ls < nb) {
-    load_rows(ls);
+    publish(lookup(ls));
     copy_rows(ls);
   }
   if (tid == 0) {
@@ -446,26 +485,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       bar_init(kfull + i, STAGE_WARPS * 32);
       bar_init(kempty + i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      bar_init(sfull + i, 1);
-      bar_init(sempty + i, SOFTMAX_WARPS * 32);
-      bar_init(xfull + i, 1);  // one local arrival with the byte count; the peer's async stores complete it
-      bar_init(xempty + i, 1);                   // the peer's exchange warp
-      bar_init(xread + i, SOFTMAX_WARPS * 32);   // this CTA's softmax threads have read the buffer
-    }
+    bar_init(sfull, 1);
+    bar_init(sempty, SOFTMAX_THREADS);
+    bar_init(qready, SOFTMAX_THREADS);
     for (int i = 0; i < NPB; ++i) {
-      bar_init(pfull + i, SOFTMAX_WARPS * 32);
+      bar_init(pfull + i, SOFTMAX_THREADS);
       bar_init(pdone + i, 1);
     }
     bar_init(odone, 1);
     bar_init(drain, 1);
-    bar_init(tdone, SOFTMAX_WARPS * 32);  // every softmax thread has made its last tensor-memory read
+    bar_init(xfull, 1);                  // one local arrival with the byte count; the peer's async stores complete it
+    bar_init(xempty, 1);                 // the peer's exchange warp
+    bar_init(xread, SOFTMAX_THREADS);    // this CTA's softmax threads have read the buffer
+    bar_init(tdone, SOFTMAX_THREADS);    // every softmax thread has made its last tensor-memory read
+    for (int i = 0; i < 4; ++i) bar_init(pmx + i, 64);  // the two softmax warps of a head quarter
     *abort_flag = 0;
     for (int i = 0; i < NSTAGE; ++i) stage_stop[i] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    // blocks 0 and 1 of the peer's partial scores are expected in exchange buffers 0 and 1
-    bar_arrive_expect(xfull + 0, X_BYTES);
-    bar_arrive_expect(xfull + 1, X_BYTES);
+    bar_arrive_expect(xfull, X_BYTES);  // block 0 of the peer's partial scores is expected in the buffer
   }
   // no key of the second half until its CTA says otherwise (it writes after the first cluster barrier)
   if (tid < HEADS) reinterpret_cast<float2*>(smem + OFF_COMB)[tid] = make_float2(-INFINITY, 0.f);
@@ -482,38 +519,47 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   cluster_sync();  // both CTAs' barriers exist before either touches the other's shared memory
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  // softmax state of head h = tid (warps 0-3), kept for the merge of the key halves after the role loops
-  const int h = tid;
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-  // this warp's 32 heads of the output half, and a shared tile for writing them (the key stages are free by then)
-  float* const orows = a.out + ((size_t)b * HEADS + (warp & 3) * 32) * DV + half * DV_HALF;
-  float* const otile = reinterpret_cast<float*>(smem + OFF_K) + (warp & 3) * 32 * 36;
+  const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+  if (warp < SOFTMAX_WARPS) {
+#pragma unroll
+    for (int c = 0; c < MAX_NDIM / 64; ++c)
+      if (4 * c < nq)
+        tmem_st16u(trow + TMEM_Q + 4 * kh * nq + 16 * c,
+                   *reinterpret_cast<const uint4(*)[4]>(qv + 4 * c));
+    tmem_wait_st();
+    tc_fence_before();
+    bar_arrive(qready);
+  }
+  // this warp's output rows (32 heads of the CTA's value half) and a shared tile for writing them (the key stages
+  // are free by then)
+  float* const orows = a.out + ((size_t)b * HEADS + q * 32) * DV + half * DV_HALF;
+  float* const otile = reinterpret_cast<float*>(smem + OFF_K) + (warp & 7) * 32 * 36;
   float m_run = -INFINITY, l_run = 0.f;
   bool sm_ok = false;
-  // with two key halves, the CTA of half s merges heads 64 s .. 64 s + 63 (softmax warps 2 s and 2 s + 1) and
+  // with two key halves, the CTA of split s merges heads 64 s .. 64 s + 63 (head quarters 2 s and 2 s + 1) and
   // hands the other heads to its counterpart
-  const bool merges = a.nsplit == 1 || (warp >> 1) == split;
+  const bool merges = a.nsplit == 1 || (q >> 1) == split;
   const unsigned lim = a.wait_limit;
 
   if (loader) {
     // ---- loaders (see above): the first block of each stage has landed; later blocks wait until the value GEMM
-    //      of the block NSTAGE earlier has read the stage. The stop decision is read after the named barrier, so
-    //      the stage's threads leave the loop together.
+    //      of the block NSTAGE earlier has read the stage. Both warps of a stage learn the outcome of the wait at a
+    //      named barrier, so they leave the loop together.
     if (ls < nb) {
       bar_arrive(kfull + ls);
       prefetch_next(ls);
     }
     for (int j = ls + NSTAGE; j < nb; j += NSTAGE) {
+      // the block's slot-list entries are read while the stage is still in use; only the copy waits for it
+      const uint8_t* r = lookup(j);
       if (lsub == 0) {
-        const bool ok = __all_sync(0xffffffffu, bar_wait(kempty + ls, (unsigned)((j / NSTAGE) - 1) & 1u, abort_flag, lim));
+        const bool ok =
+            __all_sync(0xffffffffu, bar_wait(kempty + ls, (unsigned)((j / NSTAGE) - 1) & 1u, abort_flag, lim));
         if (!ok && lane == 0) stage_stop[ls] = 1;
-        if (!ok) {
-          named_sync(1 + ls, STAGE_WARPS * 32);
-          break;
-        }
       }
-      load_rows(j);
+      named_sync(1 + ls, STAGE_WARPS * 32);
       if (stage_stop[ls]) break;
+      publish(r);
       copy_rows(j);
       prefetch_next(j);
       cp_async_wait_all();
@@ -522,16 +568,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     }
     cp_async_wait_all();
   } else if (warp == XCHG_WARP) {
-    // ---- exchange warp: once this CTA's softmax threads have read block j from exchange buffer j % 2, it expects
-    //      block j + 2 there and lets the peer send it. Its acquire (wait) and release (remote arrive) carry the
+    // ---- exchange warp: once this CTA's softmax threads have read block j from the exchange buffer, it expects
+    //      block j + 1 there and lets the peer send it. Its acquire (wait) and release (remote arrive) carry the
     //      softmax threads' reads before the peer's next stores, and keep that release off their critical path.
     if (lane == 0) {
       for (int j = 0; j < nb; ++j) {
-        const int xb = j & 1;
-        if (!bar_wait(xread + xb, (unsigned)(j >> 1) & 1u, abort_flag, lim)) break;
-        if (j + 2 < nb) {
-          bar_arrive_expect(xfull + xb, X_BYTES);
-          bar_arrive_peer(peer_addr(xempty + xb, peer));
+        if (!bar_wait(xread, (unsigned)j & 1u, abort_flag, lim)) break;
+        if (j + 1 < nb) {
+          bar_arrive_expect(xfull, X_BYTES);
+          bar_arrive_peer(peer_addr(xempty, peer));
         }
       }
     }
@@ -540,16 +585,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     // ---- one thread issues the tensor-core work: partial scores of block j over this CTA's columns, and the
     //      value GEMM of block j - 1 for this CTA's value half
     if (lane == 0) {
-      const uint32_t q0 = su32(smem + OFF_Q), k0 = su32(smem + OFF_K), p0 = su32(smem + OFF_P);
+      const uint32_t k0 = su32(smem + OFF_K), p0 = su32(smem + OFF_P), tq = tmem + TMEM_Q;
       constexpr uint32_t ID_QK = idesc_bf16(128, KB, 0, 0);
       constexpr uint32_t ID_PV = idesc_bf16(128, DV_HALF, 0, 1);
       // Descriptors are built once; an operand 256 bytes further along is the same descriptor plus 16 in its start
       // field (shared-memory addresses stay below 256 KB, so the 14-bit field never carries).
-      const uint64_t dq = sdesc(q0, 128, grp), dk = sdesc(k0, 128, grp), dp = sdesc(p0, 128, P_GROUP),
+      const uint64_t dk = sdesc(k0, 128, grp), dp = sdesc(p0, 128, P_GROUP),
                      dv = sdesc(k0, grp, 128);
       // test hook: wait on a barrier that nothing completes (drain: its only arrival is the commit below), before
       // anything is issued, so that the wait runs out with no tensor-core work or copy of this CTA in flight
       bool ok = !a.stall || bar_wait(drain, 0, abort_flag, lim);
+      ok = ok && bar_wait(qready, 0, abort_flag, lim);
       // The value GEMM of block j-1 goes in as soon as its P is ready: pfull is polled halfway through the score
       // GEMM of block j (the tensor pipe runs in issue order), so the key stage of block j-1 is released without
       // waiting for all of block j's scores.
@@ -571,27 +617,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
         bool pv_pending = j >= 1;
         const int jp = j - 1;
         if (j < nb) {
-          const int s = j % NSTAGE, sb = j & 1;
+          const int s = j % NSTAGE;
           ok = bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag, lim);
-          if (ok && j >= 2) ok = bar_wait(sempty + sb, (unsigned)((j - 2) >> 1) & 1u, abort_flag, lim);
+          // one score buffer: block j's scores go in once every softmax thread has read block j - 1's
+          if (ok && j >= 1) ok = bar_wait(sempty, (unsigned)(j - 1) & 1u, abort_flag, lim);
           if (!ok) break;
           tc_fence_after();
           const uint64_t dkb = dk + (uint64_t)((s * STAGE_BYTES) >> 4);
-          const uint32_t dst = tmem + TMEM_S + sb * KB;
+          const uint32_t dst = tmem + TMEM_S;
           constexpr int NK0 = DSPLIT / 16, NK1 = (DQK - DSPLIT) / 16;  // score MMAs of CTA 0 and CTA 1
           if (half == 0)
-            issue_qk<0, NK0 / 2>(dst, dq, dkb, ID_QK);
+            issue_qk<0, NK0 / 2>(dst, tq, dkb, ID_QK);
           else
-            issue_qk<0, NK1 / 2>(dst, dq, dkb, ID_QK);
+            issue_qk<0, NK1 / 2>(dst, tq, dkb, ID_QK);
           if (pv_pending && bar_poll(pfull + jp % NPB, (unsigned)(jp / NPB) & 1u)) {
             issue_pv(jp);
             pv_pending = false;
           }
           if (half == 0)
-            issue_qk<NK0 / 2, NK0>(dst, dq, dkb, ID_QK);
+            issue_qk<NK0 / 2, NK0>(dst, tq, dkb, ID_QK);
           else
-            issue_qk<NK1 / 2, NK1>(dst, dq, dkb, ID_QK);
-          mma_commit(sfull + sb);
+            issue_qk<NK1 / 2, NK1>(dst, tq, dkb, ID_QK);
+          mma_commit(sfull);
         }
         if (pv_pending) {
           ok = bar_wait(pfull + jp % NPB, (unsigned)(jp / NPB) & 1u, abort_flag, lim);
@@ -608,65 +655,77 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
     }
     __syncwarp();
   } else {
-    // ---- softmax: thread h = head h = TMEM lane h. The partial scores of a block go to the peer, whose partial
-    //      scores come back; both CTAs then hold S = own + peer (the same value in both, addition commutes) and
-    //      run the same softmax, so their P, running max and normaliser agree bit for bit.
+    // ---- softmax: thread h of warp w holds head h = TMEM lane h for the keys of its half (kh) of every block. The
+    //      partial scores of a block go to the peer, whose partial scores come back; both CTAs then hold S = own +
+    //      peer (the same value in both, addition commutes) and run the same softmax, so their P, running max and
+    //      normaliser agree bit for bit. The two threads of a head (warps q and q + 4) agree on the block maximum
+    //      through shared memory and a per-quarter mbarrier; each keeps the sum of its own weights.
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
-      const int s = j % NSTAGE, sb = j & 1, xb = j & 1;
-      ok = __all_sync(0xffffffffu, ok && bar_wait(sfull + sb, (unsigned)(j >> 1) & 1u, abort_flag, lim));
+      const int s = j % NSTAGE;
+      ok = __all_sync(0xffffffffu, ok && bar_wait(sfull, (unsigned)j & 1u, abort_flag, lim));
       if (!ok) break;
       tc_fence_after();
-      float sv[KB];
+      float sv[KH];
 #pragma unroll
-      for (int c = 0; c < KB; c += 16) tmem_ld16(trow + TMEM_S + sb * KB + c, *reinterpret_cast<float(*)[16]>(sv + c));
+      for (int c = 0; c < KH; c += 16)
+        tmem_ld16(trow + TMEM_S + kh * KH + c, *reinterpret_cast<float(*)[16]>(sv + c));
       tc_fence_before();
-      bar_arrive(sempty + sb);
-      // the exchange buffer xb of the peer is free once the peer has read block j - 2 from it
-      if (j >= 2) {
-        ok = __all_sync(0xffffffffu, bar_wait_cluster(xempty + xb, (unsigned)((j - 2) >> 1) & 1u, abort_flag, lim));
+      bar_arrive(sempty);
+      // the peer's exchange buffer is free once the peer has read block j - 1 from it
+      if (j >= 1) {
+        ok = __all_sync(0xffffffffu, bar_wait_cluster(xempty, (unsigned)(j - 1) & 1u, abort_flag, lim));
         if (!ok) break;
       }
-      // exchange buffer layout: float4 group g (scores 4g..4g+3) of head h at (g * HEADS + h) * 16; the stores
-      // complete the transaction bytes of the peer's xfull barrier, which the peer set up in advance
-      const uint8_t* xmine = smem + OFF_X + xb * X_BYTES;
-      const uint32_t xpeer = peer_addr(xmine + h * 16, peer), xfull_peer = peer_addr(xfull + xb, peer);
+      // exchange buffer layout: float4 group g (scores 4g..4g+3 of the block) of head h at (g * HEADS + h) * 16; the
+      // stores complete the transaction bytes of the peer's xfull barrier, which the peer set up in advance
+      const uint8_t* xmine = smem + OFF_X;
+      const uint32_t xpeer = peer_addr(xmine + h * 16, peer), xfull_peer = peer_addr(xfull, peer);
 #pragma unroll
-      for (int g = 0; g < KB / 4; ++g)
-        st_peer_async_v4(xpeer + g * HEADS * 16, sv[4 * g], sv[4 * g + 1], sv[4 * g + 2], sv[4 * g + 3], xfull_peer);
-      ok = __all_sync(0xffffffffu, bar_wait_cluster(xfull + xb, (unsigned)(j >> 1) & 1u, abort_flag, lim));
+      for (int g = 0; g < KH / 4; ++g)
+        st_peer_async_v4(xpeer + (kh * (KH / 4) + g) * HEADS * 16, sv[4 * g], sv[4 * g + 1], sv[4 * g + 2],
+                         sv[4 * g + 3], xfull_peer);
+      ok = __all_sync(0xffffffffu, bar_wait_cluster(xfull, (unsigned)j & 1u, abort_flag, lim));
       if (!ok) break;
 #pragma unroll
-      for (int g = 0; g < KB / 4; ++g) {
-        const float4 o = *reinterpret_cast<const float4*>(xmine + (g * HEADS + h) * 16);
+      for (int g = 0; g < KH / 4; ++g) {
+        const float4 o = *reinterpret_cast<const float4*>(xmine + ((kh * (KH / 4) + g) * HEADS + h) * 16);
         sv[4 * g] += o.x;
         sv[4 * g + 1] += o.y;
         sv[4 * g + 2] += o.z;
         sv[4 * g + 3] += o.w;
       }
-      bar_arrive(xread + xb);  // the exchange warp hands the buffer back to the peer
+      bar_arrive(xread);  // the exchange warp hands the buffer back to the peer
       // which keys of the block have a row (written by the loaders before they signalled the stage full)
       ok = __all_sync(0xffffffffu, bar_wait(kfull + s, (unsigned)(j / NSTAGE) & 1u, abort_flag, lim));
       if (!ok) break;
-      const uint32_t vm = kmask[s];
-      float x[KB];
+      const uint32_t vm = kmask[s * 2 + kh];
+      float x[KH];
       float mb = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < KB; ++i) {
+      for (int i = 0; i < KH; ++i) {
         x[i] = (vm >> i) & 1u ? sv[i] * a.scale_log2 : -INFINITY;
         mb = fmaxf(mb, x[i]);
       }
+      // the block maximum over both halves of the keys
+      float* const share = pshare + (j & 1) * 2 * HEADS;
+      share[kh * HEADS + h] = mb;
+      bar_arrive(pmx + q);
+      ok = __all_sync(0xffffffffu, bar_wait(pmx + q, (unsigned)j & 1u, abort_flag, lim));
+      if (!ok) break;
+      mb = fmaxf(mb, share[(kh ^ 1) * HEADS + h]);
       float m_new = m_run;
       if (mb > -INFINITY && (m_run == -INFINITY || mb > m_run + 8.f)) m_new = mb;
       const bool resc = m_new != m_run && m_run != -INFINITY;
       if (__any_sync(0xffffffffu, resc)) {
-        // O holds blocks 0 .. j-1 once the value GEMM of block j-1 has finished; scale this warp's rows
+        // O holds blocks 0 .. j-1 once the value GEMM of block j-1 has finished; scale this thread's half of its
+        // head's row (both threads of the head take the same decision)
         ok = __all_sync(0xffffffffu,
                         bar_wait(pdone + ((j - 1) % NPB), (unsigned)((j - 1) / NPB) & 1u, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
         const float f = resc ? ex2_approx(m_run - m_new) : 1.f;
-        for (int c = 0; c < DV_HALF; c += 16) {
+        for (int c = kh * (DV_HALF / 2); c < (kh + 1) * (DV_HALF / 2); c += 16) {
           float o[16];
           tmem_ld16(trow + TMEM_O + c, o);
 #pragma unroll
@@ -677,10 +736,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
         l_run *= f;
       }
       m_run = m_new;
-      uint32_t pk[KB / 2];
+      uint32_t pk[KH / 2];
       float psum = 0.f;
 #pragma unroll
-      for (int i = 0; i < KB / 2; ++i) {
+      for (int i = 0; i < KH / 2; ++i) {
         // both weights rounded to bf16 by one conversion (key 2i in the low half)
         const __nv_bfloat162 p2 =
             __floats2bfloat162_rn(x[2 * i] == -INFINITY ? 0.f : ex2_approx(x[2 * i] - m_run),
@@ -698,20 +757,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
       }
       uint8_t* prow = smem + OFF_P + pb * P_BYTES + (h >> 3) * P_GROUP + (h & 7) * 16;
 #pragma unroll
-      for (int c = 0; c < KB / 8; ++c)
-        *reinterpret_cast<uint4*>(prow + c * 128) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int c = 0; c < KH / 8; ++c)
+        *reinterpret_cast<uint4*>(prow + (kh * (KH / 8) + c) * 128) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async();
       tc_fence_before();
       bar_arrive(pfull + pb);
     }
     if (ok && nb > 0) ok = __all_sync(0xffffffffu, bar_wait(odone, 0, abort_flag, lim));
+    if (ok) {
+      // the head's normaliser: the two threads' sums (the running max is already common)
+      float* const share = pshare + (nb & 1) * 2 * HEADS;
+      share[kh * HEADS + h] = l_run;
+      bar_arrive(pmx + q);
+      ok = __all_sync(0xffffffffu, bar_wait(pmx + q, (unsigned)nb & 1u, abort_flag, lim));
+      if (ok) l_run += share[(kh ^ 1) * HEADS + h];
+    }
     sm_ok = ok;
     if (ok && !merges) {
       // heads the other key half merges: this half's normalised output goes to `out` (this CTA's columns), and
       // (m, l) to the CTA of the other half with the same columns
       tc_fence_after();
-      store_out_rows(trow, nb > 0, l_run > 0.f ? 1.f / l_run : 0.f, 0.f, otile, orows, lane);
-      st_peer_v2(peer_addr(smem + OFF_COMB + h * 8, rank ^ 2u), m_run, l_run);
+      store_out_rows(trow, nb > 0, l_run > 0.f ? 1.f / l_run : 0.f, 0.f, otile, orows, lane, kh * (DV_HALF / 2));
+      if (kh == 0) st_peer_v2(peer_addr(smem + OFF_COMB + h * 8, rank ^ 2u), m_run, l_run);
     }
   }
 
@@ -719,18 +787,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) hs_mla_decode_kernel(const MlaArg
   __syncthreads();
   cluster_sync();  // the peers no longer touch this CTA's shared memory, and the second half's outputs are written
   if (warp < SOFTMAX_WARPS && sm_ok && merges) {
-      // merge with the other key half (none: m1 = -inf, l1 = 0): with M = max(m0, m1) and c_s = 2^(m_s - M),
-      // out = (c0 O0 + c1 l1 out1) / (c0 l0 + c1 l1), lse = ln 2 * (M + log2(c0 l0 + c1 l1))
-      tc_fence_after();
-      const float2 ml1 = *reinterpret_cast<const float2*>(smem + OFF_COMB + h * 8);
-      const float m1 = a.nsplit > 1 ? ml1.x : -INFINITY, l1 = a.nsplit > 1 ? ml1.y : 0.f;
-      const float mx = fmaxf(m_run, m1);
-      const float c0 = l_run > 0.f ? ex2_approx(m_run - mx) : 0.f, c1 = l1 > 0.f ? ex2_approx(m1 - mx) : 0.f;
-      const float lsum = c0 * l_run + c1 * l1;
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      store_out_rows(trow, nb > 0, c0 * inv, c1 * l1 * inv, otile, orows, lane);
-      if (half == 0)
-        a.lse[(size_t)b * HEADS + h] = lsum > 0.f ? (mx + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+    // merge with the other key half (none: m1 = -inf, l1 = 0): with M = max(m0, m1) and c_s = 2^(m_s - M),
+    // out = (c0 O0 + c1 l1 out1) / (c0 l0 + c1 l1), lse = ln 2 * (M + log2(c0 l0 + c1 l1))
+    tc_fence_after();
+    const float2 ml1 = *reinterpret_cast<const float2*>(smem + OFF_COMB + h * 8);
+    const float m1 = a.nsplit > 1 ? ml1.x : -INFINITY, l1 = a.nsplit > 1 ? ml1.y : 0.f;
+    const float mx = fmaxf(m_run, m1);
+    const float c0 = l_run > 0.f ? ex2_approx(m_run - mx) : 0.f, c1 = l1 > 0.f ? ex2_approx(m1 - mx) : 0.f;
+    const float lsum = c0 * l_run + c1 * l1;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    store_out_rows(trow, nb > 0, c0 * inv, c1 * l1 * inv, otile, orows, lane, kh * (DV_HALF / 2));
+    if (half == 0 && kh == 0)
+      a.lse[(size_t)b * HEADS + h] = lsum > 0.f ? (mx + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
   }
   // The tensor memory is freed once every softmax thread has arrived on tdone after its last read of it (a
   // per-thread arrival count: a CTA-wide bar.sync here was seen to let the other warps through while two warps
