@@ -720,6 +720,9 @@ def roofline_of(w, mode, env: Env, n_launch_layers: int, n_kernels: int, tot, ke
     """Roofline of the resolve kernel over a pass: link term (miss bytes over the measured link) and HBM term
     (metadata + hot-buffer bytes; in no-IO mode the rows are read from HBM too), over the measured time."""
     hits, misses, evictions, miss_bytes = (int(x) for x in tot)
+    # the committed captures are of the plain per-layer resolve; no other mode's launches are what they measured
+    plain = not any(mode.get(k) for k in ("prefetch", "shared_call", "full_offload", "work_only", "tiered_frac",
+                                          "attention", "layer_work_mb"))
     if mode.get("full_offload"):  # every selected row crossed the link
         hits, misses = 0, n_launch_layers * w.requests * w.topk
         miss_bytes = misses * w.row_bytes
@@ -733,7 +736,7 @@ def roofline_of(w, mode, env: Env, n_launch_layers: int, n_kernels: int, tot, ke
         return {"bound": "hbm", "achieved": hbm / kern_s / 1e9, "peak": env.hbm_peak, "unit": "GB/s",
                 "frac": hbm / (env.hbm_peak * 1e9) / kern_s, "hbm_bytes_per_launch": hbm / n_kernels,
                 "traffic": captured_traffic(w, sum(w.layers for r in rows if r[0] == 0),
-                                            sum(w.layers for r in rows if r[0] != 0), noio=True),
+                                            sum(w.layers for r in rows if r[0] != 0), noio=True) if plain else None,
                 "peak_source": f"HBM {env.hbm_peak:.1f} GB/s {env.hbm_src} (MEASURED_PEAKS.json copy)"}
     hbm = meta + miss_bytes
     t_link = miss_bytes / (link_peak * 1e9)
@@ -747,15 +750,17 @@ def roofline_of(w, mode, env: Env, n_launch_layers: int, n_kernels: int, tot, ke
         "frac": max(t_link, t_hbm) / kern_s,
         "hbm_frac": t_hbm / kern_s,
         "traffic": captured_traffic(w, sum(w.layers for r in rows if r[0] == 0),
-                                    sum(w.layers for r in rows if r[0] != 0)),
+                                    sum(w.layers for r in rows if r[0] != 0)) if plain else None,
         "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed ncu capture "
                           "(profiles/) of this workload's steady launches, null unless taken on these kernel sources",
-        "kernel": "hs_resolve_kernel",
+        "kernel": "hs_gather_kernel" if mode.get("full_offload") else "hs_resolve_kernel",
         "kernel_ms_per_launch": kern_ms / n_kernels,
         "launches": n_kernels,
-        "timing": ("CUDA events around each step's graph in the timed region: hs_step_begin plus the step's "
-                   "resolves, an upper bound on the resolve launches" +
-                   (" (layer-wise prefetch on a second stream included)" if mode.get("prefetch") else "")),
+        "timing": ("CUDA events around each step's graph in the timed region: " +
+                   ("the step's hs_gather_history launches (every selected row of every layer from host memory)"
+                    if mode.get("full_offload") else
+                    "the step increment plus the step's resolves, an upper bound on the resolve launches" +
+                    (" (layer-wise prefetch on side streams included)" if mode.get("prefetch") else ""))),
         "algorithmic_bytes_per_launch": {"link": miss_bytes / n_kernels, "hbm": hbm / n_kernels},
         "peak_source": f"host link measured in this run (zero-copy {link[0]:.1f}, memcpy {link[1]:.1f} GB/s); "
                        f"HBM {env.hbm_peak:.1f} GB/s {env.hbm_src}",
