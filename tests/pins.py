@@ -4,9 +4,10 @@ Each pin raises AssertionError when the oracle under test disagrees with it. The
 real oracle (all must pass) and against deliberately broken copies of it (each copy must fail at least one), which
 shows the pins can catch a plausible mistake anywhere in the oracle.
 
-The policy being pinned is the per-layer resolution of the HiSparse paper (Abstract: hit detection, LRU
-replacement and host-to-device fetches; outputs unchanged because only KV placement changes) with the stated
-readings: stamp = decode step, oldest stamp first, ties to the lowest slot, misses paired with victims in
+The policy being pinned is the per-layer resolution of "HiSparse: Scaling Sparse-Attention Decoding with
+Hierarchical KV Cache Management" (Abstract): per layer, find which selected tokens are already cached, choose
+least recently used victims for the rest and bring their rows over from the host, which moves KV rows without
+changing what attention reads. The stated readings: stamp = decode step, oldest stamp first, ties to the lowest slot, misses paired with victims in
 ascending token order, empties (stamp 0) first, rows with out-of-range or duplicate tokens rejected whole.
 """
 from __future__ import annotations
