@@ -55,3 +55,32 @@ def test_committed_captures_name_their_sources():
         assert len(cap[key]) == 16 and int(cap[key], 16) >= 0
         assert cap["command"].startswith("ncu ") and "--clock-control none" in cap["command"]
         assert "_work" not in cap["command"]
+
+
+class _Env:
+    hbm_peak = 6789.6
+    hbm_src = "measured"
+
+
+class _Res:
+    res = None  # no resident maps
+
+
+def test_only_the_plain_resolve_carries_captured_traffic(tmp_path, monkeypatch):
+    """The committed captures are of the plain per-layer resolve: a full-offload pass (the gather kernel), a
+    prefetch pipeline or a shared call must not borrow their DRAM bytes."""
+    w = wl.WORKLOADS["dsa"]
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    cap = {"kernel_sources_sha16": bench.kernel_sources_sha16(), "dram_bytes_per_launch": {"cold": None, "steady": 100}}
+    _write(tmp_path, f"hs_resolve_kernel_{w.name}_ncu.json", cap)
+    rows = [(0, 1.0, None), (1, 1.0, None)]
+    tot = [1000, 100, 50, 100 * w.row_bytes]
+    args = (2, 2, tot, 2.0, (200.0, 200.0), _Res(), rows)
+    plain = bench.roofline_of(w, {}, _Env(), *args)
+    assert plain["traffic"] == 100 and plain["kernel"] == "hs_resolve_kernel"
+    off = bench.roofline_of(w, {"full_offload": True}, _Env(), *args)
+    assert off["traffic"] is None and off["kernel"] == "hs_gather_kernel"
+    assert "hs_gather_history" in off["timing"]
+    for mode in ({"prefetch": True}, {"shared_call": True}, {"tiered_frac": 0.3}):
+        assert bench.roofline_of(w, mode, _Env(), *args)["traffic"] is None, mode
+    assert bench.roofline_of(w, {"prefetch": True}, _Env(), *args, noio=True)["traffic"] is None
