@@ -16,7 +16,8 @@
 // selected row, CTA 1 columns 256..575. Each computes partial scores over its columns on the tensor cores, sends
 // them to the other through distributed shared memory, and adds the other's. Both then hold the same S (addition
 // commutes), run the same softmax, and each multiplies P by its own value half (columns 0..255 or 256..511, which
-// lie within its columns). Half of Q per CTA leaves room for four key stages, and no score work is repeated.
+// lie within its columns). No score work is repeated. Each CTA keeps its columns of Q in tensor memory, as the
+// score GEMM's A operand, which leaves shared memory to four key stages.
 // A request's keys are split in two as well (two pairs, a cluster of four CTAs) whenever every request's cluster
 // fits on the device at once: each pair runs the softmax over its half of the key blocks, and each merges half of
 // the heads (flash-decoding's split-K merge, inside one cluster): for the other heads a pair writes its normalised
@@ -28,23 +29,25 @@
 //               w / 4 of every 64-key block; the two threads of a head agree on the block maximum through shared
 //               memory and an mbarrier, and each sums its own weights;
 //   warp 8      lane 0 issues every tcgen05.mma (and warp 8 allocates / frees the tensor memory);
-//   warps 9-12  load the CTA's columns of the selected rows into shared memory with cp.async (zero rows for
+//   warps 9-16  load the CTA's columns of the selected rows into shared memory with cp.async (zero rows for
 //               padding), 64 rows per block, two warps per key stage (one per half of the block's keys),
 //               prefetching each stage's next rows into L2;
-//   warp 13     hands the score-exchange buffer back to the peer once it has been read.
-// Shared memory: this CTA's columns of Q (128 x 256 or 320), two key stages (64 rows each), one P buffer and one
-// exchange buffer, in the no-swizzle interleaved layout: element (row r, column c) at (r/8)*G + (c/8)*128 +
+//   warp 17     hands the score-exchange buffer back to the peer once it has been read.
+// Shared memory: four key stages (64 rows each), one P buffer and one exchange buffer, in the no-swizzle
+// interleaved layout: element (row r, column c) at (r/8)*G + (c/8)*128 +
 // (r%8)*16 + (c%8)*2, where G is the byte size of an 8-row group (one spare 128-byte slot included). A key stage
 // serves the score GEMM as a K-major operand (rows = keys) and the value GEMM as an MN-major operand (the same
 // bytes read with the two strides exchanged).
-// Tensor memory (512 columns): two 64-column score buffers, and the 256-column output half at column 256.
-// Per key block j: partial S = Q K^T (16 or 20 MMAs of 128x64x16) into score buffer j%2; the softmax threads
-// read it, store it into the peer's exchange buffer with st.async (completing the bytes the peer's barrier
-// expects), wait for the peer's part, and update the running max m (raised only when a block's maximum exceeds
+// Tensor memory (512 columns): this CTA's columns of Q (two bf16 per column, up to 160 columns), one 64-column
+// score buffer at column 192, and the 256-column output half at column 256.
+// Per key block j: partial S = Q K^T (16 or 20 MMAs of 128x64x16, A from tensor memory) into the score buffer; the
+// softmax threads read it, store it into the peer's exchange buffer with st.async (completing the bytes the peer's
+// barrier expects), wait for the peer's part, and update the running max m (raised only when a block's maximum exceeds
 // it by more than 8 in log2 units, which bounds P and O by 2^8 and makes the rescale of O rare); they write
 // P = 2^(s - m) rounded to bf16 into the P buffer once the value GEMM of block j-1 has read it, and sum the
-// rounded values; then O += P V (four 128x256x16 MMAs). The score GEMM of block j+1 overlaps the softmax of
-// block j. The output leaves through a shared tile in whole 128-byte row segments. mbarriers order the roles,
+// rounded values; then O += P V (four 128x256x16 MMAs). The score GEMM of block j+1 starts as soon as the
+// softmax threads have read block j's scores, and overlaps the rest of block j's softmax. The output leaves
+// through a shared tile in whole 128-byte row segments. mbarriers order the roles,
 // within the CTA and across the pair; every wait is bounded: on running out
 // it sets an abort flag that ends every role and the HS_DEVERR_TIMEOUT bit of the pool's error word, after the
 // issued MMAs and copies have drained. Cluster barriers at the start and the end keep each CTA's shared memory
