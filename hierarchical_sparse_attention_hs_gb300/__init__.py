@@ -23,6 +23,7 @@ __all__ = [
     "HS_DEVERR_STATE", "HostBuffer", "PoolBuffers", "hs_probe_link", "hs_gather", "hs_gather_history",
     "hs_resolve_shared", "hs_resolve_tiered", "hs_mla_decode", "hs_mla_decode_history", "HS_DEVERR_TIMEOUT",
     "MLA_HEADS", "MLA_D_QK", "MLA_D_V", "hs_probe_launch", "hs_debug_attention", "hs_step_begin_fused", "hs_probe_link_static", "HS_ERR_TOO_LARGE",
+    "hs_resolve_ids", "hs_prefetch_ids",
 ]
 
 HS_OK = 0
@@ -82,6 +83,8 @@ def load():
             "hs_step_begin_fused": (ctypes.c_int, [vp]),
             "hs_resolve": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp]),
             "hs_prefetch": (ctypes.c_int, [vp, i32, i32, vp, i32, vp]),
+            "hs_resolve_ids": (ctypes.c_int, [vp, i32, i32, vp, vp, i32, vp, vp]),
+            "hs_prefetch_ids": (ctypes.c_int, [vp, i32, i32, vp, vp, i32, vp]),
             "hs_gather": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp]),
             "hs_resolve_shared": (ctypes.c_int, [vp, i32, i32, i32, vp, i32, vp, vp]),
             "hs_resolve_tiered": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, ctypes.c_int64, vp, vp]),
@@ -199,6 +202,16 @@ def hs_resolve(pool: int, layer: int, batch: int, topk_idx, k: int, out_slots, s
 
 def hs_prefetch(pool: int, layer: int, batch: int, topk_idx, k: int, stream=None) -> None:
     _check(load().hs_prefetch(pool, layer, batch, _addr(topk_idx), k, _stream(stream)), "hs_prefetch")
+
+
+def hs_resolve_ids(pool: int, layer: int, batch: int, req_ids, topk_idx, k: int, out_slots, stream=None) -> None:
+    _check(load().hs_resolve_ids(pool, layer, batch, _addr(req_ids), _addr(topk_idx), k, _addr(out_slots),
+                                 _stream(stream)), "hs_resolve_ids")
+
+
+def hs_prefetch_ids(pool: int, layer: int, batch: int, req_ids, topk_idx, k: int, stream=None) -> None:
+    _check(load().hs_prefetch_ids(pool, layer, batch, _addr(req_ids), _addr(topk_idx), k, _stream(stream)),
+           "hs_prefetch_ids")
 
 
 def hs_resolve_shared(pool: int, layer0: int, nlayers: int, batch: int, topk_idx, k: int, out_slots,

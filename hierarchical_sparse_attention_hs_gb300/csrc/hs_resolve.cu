@@ -100,6 +100,8 @@ struct ResolveArgs {
   int64_t resident_stride;
   int32_t nlayers;
   int32_t groups;                // layer groups: cluster (b, g) handles request b for the g-th run of layers
+  const int32_t* req_ids;        // [batch] pool request of each batch row, or nullptr (row b is request b)
+  int32_t max_batch;             // pool requests (valid request ids are 0 .. max_batch-1)
   int64_t meta_layer_ctx;        // int32 elements between layers in tok2slot
   int64_t meta_layer_slots;      // int32 elements between layers in slot_tok / slot_stamp
   int64_t src_layer_bytes;       // bytes between layers in the row source
@@ -303,15 +305,30 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
       *a.done = 0;
     }
   };
-  int32_t* t2s = a.tok2slot + (size_t)l0 * (size_t)a.meta_layer_ctx + (size_t)b * ctx;
-  int32_t* s2t = a.slot_tok + (size_t)l0 * (size_t)a.meta_layer_slots + (size_t)b * H;
-  int32_t* stp = a.slot_stamp + (size_t)l0 * (size_t)a.meta_layer_slots + (size_t)b * H;
-  unsigned long long* counters = a.counters + 4 * (size_t)l0;
   const int32_t* sel = a.topk + (size_t)b * k;
   int32_t* out = (a.out_slots && grp == 0) ? a.out_slots + (size_t)b * k : nullptr;  // identical in every group
-  const uint8_t* src = a.src + (size_t)l0 * (size_t)a.src_layer_bytes + (size_t)b * (size_t)a.src_req_stride;
+  // The pool request of batch row b: req_ids[b] when the call maps rows to requests, else b. A row whose id is
+  // out of range is rejected whole before any of the pool's memory is read (every CTA of the cluster reads the
+  // same id and leaves here, before any barrier of the cluster).
+  int rq = b;
+  if (a.req_ids) {
+    rq = ld_fresh(a.req_ids + b);
+    if (rq < 0 || rq >= a.max_batch) {
+      if (out)
+        for (int i = tid; i < k; i += NT)
+          if (((i >> 5) % C) == rank) out[i] = -1;
+      if (rank == 0 && tid == 0) atomicOr(a.err, (int)HS_DEVERR_RANGE);
+      finish();
+      return;
+    }
+  }
+  int32_t* t2s = a.tok2slot + (size_t)l0 * (size_t)a.meta_layer_ctx + (size_t)rq * ctx;
+  int32_t* s2t = a.slot_tok + (size_t)l0 * (size_t)a.meta_layer_slots + (size_t)rq * H;
+  int32_t* stp = a.slot_stamp + (size_t)l0 * (size_t)a.meta_layer_slots + (size_t)rq * H;
+  unsigned long long* counters = a.counters + 4 * (size_t)l0;
+  const uint8_t* src = a.src + (size_t)l0 * (size_t)a.src_layer_bytes + (size_t)rq * (size_t)a.src_req_stride;
   const int32_t* res = a.resident ? a.resident + (size_t)b * (size_t)a.resident_stride : nullptr;
-  uint8_t* hot = a.hot + (size_t)l0 * (size_t)a.hot_layer_bytes + (size_t)b * (size_t)H * (size_t)R;
+  uint8_t* hot = a.hot + (size_t)l0 * (size_t)a.hot_layer_bytes + (size_t)rq * (size_t)H * (size_t)R;
   const int hwords = (H + 31) >> 5;
   const int cwords = (ctx + 31) >> 5;
   const int cpr = R >> 4;
@@ -962,7 +979,7 @@ int pick_cluster(const hs_pool* p, int batch, bool prefetch) {
 
 int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk, int32_t k, int32_t* out,
                    cudaStream_t s, int32_t nlayers = 1, const int32_t* resident = nullptr,
-                   int64_t resident_stride = 0, bool empty = false) {
+                   int64_t resident_stride = 0, bool empty = false, const int32_t* req_ids = nullptr) {
   if (!p || layer < 0 || nlayers < 1 || layer > p->d.layers - nlayers || batch < 0 || batch > p->d.max_batch ||
       k < 0 || k > p->d.topk_max)
     return HS_ERR_INVALID_ARG;
@@ -1016,6 +1033,8 @@ int launch_resolve(hs_pool* p, int32_t layer, int32_t batch, const int32_t* topk
   }
   a.resident = resident;
   a.resident_stride = resident_stride;
+  a.req_ids = req_ids;
+  a.max_batch = p->d.max_batch;
   a.meta_layer_ctx = (int64_t)p->d.max_batch * p->d.ctx;
   a.meta_layer_slots = (int64_t)p->d.max_batch * p->d.slots;
   a.src_layer_bytes = p->d.host_layer_stride;
@@ -1202,6 +1221,20 @@ int hs_resolve(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* topk_
 int hs_prefetch(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* topk_idx, int32_t k,
                 hs_stream_t stream) {
   return launch_resolve(pool, layer, batch, topk_idx, k, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int hs_resolve_ids(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* req_ids, const int32_t* topk_idx,
+                   int32_t k, int32_t* out_slots, hs_stream_t stream) {
+  if (batch > 0 && k > 0 && (!out_slots || !req_ids)) return HS_ERR_INVALID_ARG;
+  return launch_resolve(pool, layer, batch, topk_idx, k, out_slots, reinterpret_cast<cudaStream_t>(stream), 1,
+                        nullptr, 0, false, req_ids);
+}
+
+int hs_prefetch_ids(hs_pool* pool, int32_t layer, int32_t batch, const int32_t* req_ids, const int32_t* topk_idx,
+                    int32_t k, hs_stream_t stream) {
+  if (batch > 0 && k > 0 && !req_ids) return HS_ERR_INVALID_ARG;
+  return launch_resolve(pool, layer, batch, topk_idx, k, nullptr, reinterpret_cast<cudaStream_t>(stream), 1,
+                        nullptr, 0, false, req_ids);
 }
 
 static int launch_gather(hs_pool* p, int32_t layer, int32_t batch, const int32_t* idx, int32_t k, void* dst,

@@ -181,6 +181,23 @@ int hs_prefetch(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk
                 hs_stream_t stream);
 
 /*
+ * hs_resolve and hs_prefetch with a request-id indirection: batch row b (row b of topk_idx and out_slots) is
+ * resolved against pool request req_ids[b] instead of request b, so a serving engine whose batch rows are not its
+ * cache slots passes its mapping instead of permuting the pool. Basis: the paper keeps one cache per request
+ * (Abstract); which request a batch row belongs to is the engine's, and the plain reading is a per-row request id.
+ *   req_ids: int32 [batch], device or mapped host memory, read once per call; every id in 0 .. max_batch-1 and
+ *     distinct within a call (two rows with one id would update that request's metadata concurrently: not
+ *     checked, like the distinct tokens of a row). A row whose id is out of range is rejected whole before any of
+ *     the pool is read: its out_slots are -1 and the error word gets HS_DEVERR_RANGE; the other rows proceed.
+ *   Everything else as hs_resolve / hs_prefetch (the per-request host pool rows and hot-buffer slots are those of
+ *   request req_ids[b]); HS_ERR_INVALID_ARG also for a null req_ids.
+ */
+int hs_resolve_ids(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *req_ids, const int32_t *topk_idx,
+                   int32_t k, int32_t *out_slots, hs_stream_t stream);
+int hs_prefetch_ids(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *req_ids, const int32_t *topk_idx,
+                    int32_t k, hs_stream_t stream);
+
+/*
  * One resolve for `nlayers` consecutive layers layer0 .. layer0+nlayers-1 that share one selection per request
  * (the models for which the HiSparse paper, Abstract, prefetches layer by layer). Layers that are always resolved
  * together with the same selection hold identical metadata, so the victims are worked out once, from layer0, and
