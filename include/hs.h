@@ -30,13 +30,14 @@
  * errors that only the device can see (a bad token) never trap: they set bits of the device error word, read
  * with hs_get_error.
  *
- * Streams and graphs: hs_pool_create, hs_pool_reset, hs_step_begin, hs_resolve and hs_prefetch only enqueue work
- * on the given stream (no host synchronisation) and can be captured into a CUDA graph. The kernels use
+ * Streams and graphs: hs_pool_create, hs_pool_reset, hs_step_begin and the resolve calls (hs_resolve, hs_prefetch,
+ * their _ids forms, hs_resolve_shared, hs_resolve_tiered) only enqueue work on the given stream (no host
+ * synchronisation) and can be captured into a CUDA graph. The kernels use
  * programmatic dependent launch: each waits for the preceding kernel in its stream before touching memory.
  * Pointers, batch and k are baked into a captured graph; refill topk_idx in place between replays.
  * The hs_get_* readers synchronise the device. No function is thread-safe on the same pool.
  *
- * Where the per-call arrays may live: topk_idx, resident_row and out_slots may be device memory or page-locked
+ * Where the per-call arrays may live: topk_idx, req_ids, resident_row and out_slots may be device memory or page-locked
  * host memory mapped into the device's address space (hs_host_alloc, or cudaHostAlloc with
  * cudaHostAllocMapped; pass the device-side address, which equals the host address under unified addressing,
  * as on GB300). The kernels then read the selection and write the slots over the host link (NVLink-C2C)
@@ -164,8 +165,8 @@ int hs_step_begin_fused(hs_pool *pool);
  * Resolve one layer's selections for requests 0..batch-1 (batch row b is pool request b) at the current step:
  * hit test, LRU victim choice, metadata update and the fetch of every missing row into its hot slot, in one
  * kernel ("HiSparse" paper, Abstract). topk_idx: int32 [batch][k], row-major; out_slots: int32 [batch][k],
- * written in input order (device or mapped host memory, see above). 1 <= batch <= max_batch, 1 <= k <= topk_max; batch == 0 or k == 0 is a
- * no-op. Enqueued on `stream`.
+ * written in input order (device or mapped host memory, see above). 1 <= batch <= max_batch,
+ * 1 <= k <= topk_max; batch == 0 or k == 0 is a no-op. Enqueued on `stream`.
  */
 int hs_resolve(hs_pool *pool, int32_t layer, int32_t batch, const int32_t *topk_idx, int32_t k,
                int32_t *out_slots, hs_stream_t stream);
