@@ -295,6 +295,23 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   const int nl = min(a.nlayers, l0 + lgrp) - l0;  // >= 1: the host makes at most nlayers groups
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = a.k, H = a.slots, ctx = a.ctx, R = a.row_bytes;
+  // Each warp handles a contiguous run of selection entries in steps 2 and 3. The first entries of its run are
+  // requested before anything else: the hit test waits on them and then on the token map, two round trips to
+  // memory that the rest of the prologue overlaps.
+  const int32_t* sel = a.topk + (size_t)b * k;
+  const int wseg = ((k + NW * 32 - 1) / (NW * 32)) * 32;
+  const int wbeg = min(k, warp * wseg);
+  const int wend = min(k, wbeg + wseg);
+  constexpr int RUN_STEP = 4 * 32;  // entries of a warp's run per iteration
+  int32_t tn[4];
+  auto load_sel = [&](int i0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * 32 + lane;
+      tn[u] = i < wend ? ld_fresh(sel + i) : -1;
+    }
+  };
+  load_sel(wbeg);
   const int32_t step = __ldcg(a.step) + a.begin;
   // On every way out: the last CTA of a step-beginning launch publishes the advanced step. Only the reads of the
   // old value must come first, and every thread of a CTA has read it (and used it) long before its thread 0 gets
@@ -305,7 +322,6 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
       *a.done = 0;
     }
   };
-  const int32_t* sel = a.topk + (size_t)b * k;
   int32_t* out = (a.out_slots && grp == 0) ? a.out_slots + (size_t)b * k : nullptr;  // identical in every group
   // The pool request of batch row b: req_ids[b] when the call maps rows to requests, else b. A row whose id is
   // out of range is rejected whole before any of the pool's memory is read (every CTA of the cluster reads the
@@ -336,13 +352,9 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
   // which write their metadata and out_slots. Row chunks go in blocks of BLK: block g belongs to CTA g % C.
   constexpr int BLK = 32 * COPY_UNROLL;
   auto owned = [&](int i) { return ((i >> 5) % C) == rank; };
-  // Each warp handles a contiguous run of selection entries in steps 2 and 3.
-  const int wseg = ((k + NW * 32 - 1) / (NW * 32)) * 32;
-  const int wbeg = min(k, warp * wseg);
-  const int wend = min(k, wbeg + wseg);
 
   // 1. the slot metadata starts on its way to shared memory (asynchronous copies, waited for at the end of step
-  //    2), the first entries of this warp's run of the selection are loaded, and the bitmaps are cleared
+  //    2), and the bitmaps are cleared
   unsigned bad = 0;
   if ((H & 3) == 0) {  // per-request arrays start on 16-byte boundaries
     for (int c = tid; c < (H >> 2); c += NT) {
@@ -356,16 +368,6 @@ __global__ void __launch_bounds__(NT, 1) hs_resolve_kernel(const ResolveArgs a) 
     }
   }
   cp_async_commit();
-  constexpr int RUN_STEP = 4 * 32;  // entries of a warp's run per iteration
-  int32_t tn[4];
-  auto load_sel = [&](int i0) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * 32 + lane;
-      tn[u] = i < wend ? ld_fresh(sel + i) : -1;
-    }
-  };
-  load_sel(wbeg);
   if (tid < MISC_INTS) s_misc[tid] = 0;
   for (int w = tid; w < hwords; w += NT) s_hit[w] = 0u;
   if (BITMAP)
