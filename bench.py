@@ -62,11 +62,11 @@ DEFAULT_SET = [("shared", {"prefetch": True, "prefetch_depth": 2}), ("shared", {
 HIDING_WORK_MB = 64.0  # per-layer work stand-in of the prefetch-hiding measurement on the headline workload
 # Before a timed pass the stream first runs a spin of this many GPU cycles (about 97 ms at 2.07 GHz), outside the
 # timed intervals: the host then enqueues every step of the pass while the GPU is still busy, so a stall of the host
-# thread (the GPU machine is a shared VM) cannot fall between a step's start event and its graph launch. A 5 ms spin
-# was seen to run out on a pass whose host thread took about 1 ms per step to enqueue, and the steps after that
-# point then measured the host (0.2-1 ms each against 0.05 ms); stalls of more than 48 ms were seen too. (A kernel
-# that holds the stream until the host releases it does not serve: with the GPU held, the launch queue fills and
-# the host blocks before it can release, and first launches wait for the device to go idle.)
+# thread (the host may be a shared virtual machine) cannot fall between a step's start event and its graph launch. A
+# 5 ms spin was seen to run out on a pass whose host thread took about 1 ms per step to enqueue, and the steps after
+# that point then measured the host (0.2-1 ms each against 0.05 ms); stalls of more than 48 ms were seen too. (A
+# kernel that holds the stream until the host releases it does not serve: with the GPU held, the launch queue fills
+# and the host blocks before it can release, and first launches wait for the device to go idle.)
 LEAD_CYCLES = 200_000_000
 
 

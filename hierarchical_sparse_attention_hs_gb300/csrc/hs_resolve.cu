@@ -1368,7 +1368,7 @@ int hs_probe_link(const void* host, void* dev, size_t bytes, int32_t iters, hs_s
   }
   int rc = HS_OK;
   float best_zc = 1e30f, best_cp = 1e30f, ms = 0.f;
-  for (int r = 0; r <= iters && rc == HS_OK; ++r) {  // round 0 warms up
+  for (int r = 0; r <= iters && rc == HS_OK; ++r) {  // iteration 0 warms up
     if (cudaEventRecord(e0, s) != cudaSuccess) rc = HS_ERR_CUDA;
     hs_probe_read_kernel<<<2 * sms, 512, 0, s>>>(static_cast<const uint8_t*>(dhost), bytes >> 4,
                                                   static_cast<unsigned*>(dev));
@@ -1469,7 +1469,7 @@ extern "C" int hs_probe_link_static(const void* host, size_t bytes, int32_t iter
     return HS_ERR_CUDA;
   // The same two transfers as hs_probe_link, timed by device clock stamps written into the scratch (no events).
   unsigned long long best_zc = ~0ull, best_cp = ~0ull;
-  for (int r = 0; r <= iters; ++r) {  // round 0 warms up
+  for (int r = 0; r <= iters; ++r) {  // iteration 0 warms up
     hs_clock_stamp_kernel<<<1, 1, 0, s>>>(stamps + 0);
     hs_probe_read_kernel<<<2 * sms, 512, 0, s>>>(static_cast<const uint8_t*>(dhost), bytes >> 4,
                                                   reinterpret_cast<unsigned*>(scratch));
