@@ -68,6 +68,7 @@ HIDING_WORK_MB = 64.0  # per-layer work stand-in of the prefetch-hiding measurem
 # kernel that holds the stream until the host releases it does not serve: with the GPU held, the launch queue fills
 # and the host blocks before it can release, and first launches wait for the device to go idle.)
 LEAD_CYCLES = 200_000_000
+HBM_NOMINAL_GBS = 8000.0  # the nominal HBM3e rate ("about 8 TB/s"), reported beside the measured copy peak
 
 
 def describe(w: wl.Workload) -> str:
@@ -736,10 +737,12 @@ def roofline_of(w, mode, env: Env, n_launch_layers: int, n_kernels: int, tot, ke
     if noio:
         hbm = meta + 2 * miss_bytes
         return {"bound": "hbm", "achieved": hbm / kern_s / 1e9, "peak": env.hbm_peak, "unit": "GB/s",
-                "frac": hbm / (env.hbm_peak * 1e9) / kern_s, "hbm_bytes_per_launch": hbm / n_kernels,
+                "frac": hbm / (env.hbm_peak * 1e9) / kern_s,
+                "frac_of_nominal": hbm / (HBM_NOMINAL_GBS * 1e9) / kern_s, "hbm_bytes_per_launch": hbm / n_kernels,
                 "traffic": captured_traffic(w, sum(w.layers for r in rows if r[0] == 0),
                                             sum(w.layers for r in rows if r[0] != 0), noio=True) if plain else None,
-                "peak_source": f"HBM {env.hbm_peak:.1f} GB/s {env.hbm_src} (MEASURED_PEAKS.json copy)"}
+                "peak_source": f"HBM {env.hbm_peak:.1f} GB/s {env.hbm_src} (MEASURED_PEAKS.json copy); "
+                               f"frac_of_nominal: against {HBM_NOMINAL_GBS:.0f} GB/s nominal"}
     hbm = meta + miss_bytes
     t_link = miss_bytes / (link_peak * 1e9)
     t_hbm = hbm / (env.hbm_peak * 1e9)
@@ -751,6 +754,7 @@ def roofline_of(w, mode, env: Env, n_launch_layers: int, n_kernels: int, tot, ke
         "unit": "GB/s",
         "frac": max(t_link, t_hbm) / kern_s,
         "hbm_frac": t_hbm / kern_s,
+        "hbm_frac_of_nominal": hbm / (HBM_NOMINAL_GBS * 1e9) / kern_s,
         "traffic": captured_traffic(w, sum(w.layers for r in rows if r[0] == 0),
                                     sum(w.layers for r in rows if r[0] != 0)) if plain else None,
         "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed ncu capture "
@@ -765,7 +769,8 @@ def roofline_of(w, mode, env: Env, n_launch_layers: int, n_kernels: int, tot, ke
                     (" (layer-wise prefetch on side streams included)" if mode.get("prefetch") else ""))),
         "algorithmic_bytes_per_launch": {"link": miss_bytes / n_kernels, "hbm": hbm / n_kernels},
         "peak_source": f"host link measured in this run (zero-copy {link[0]:.1f}, memcpy {link[1]:.1f} GB/s); "
-                       f"HBM {env.hbm_peak:.1f} GB/s {env.hbm_src}",
+                       f"HBM {env.hbm_peak:.1f} GB/s {env.hbm_src} (hbm_frac_of_nominal: against "
+                       f"{HBM_NOMINAL_GBS:.0f} GB/s nominal)",
     }
 
 

@@ -84,3 +84,17 @@ def test_only_the_plain_resolve_carries_captured_traffic(tmp_path, monkeypatch):
     for mode in ({"prefetch": True}, {"shared_call": True}, {"tiered_frac": 0.3}):
         assert bench.roofline_of(w, mode, _Env(), *args)["traffic"] is None, mode
     assert bench.roofline_of(w, {"prefetch": True}, _Env(), *args, noio=True)["traffic"] is None
+
+
+def test_hbm_fractions_against_measured_and_nominal_peaks():
+    """The HBM term is reported against the measured copy peak and, beside it, the nominal rate: the same bytes over
+    the same time, so the two fractions differ by exactly the ratio of the peaks."""
+    w = wl.WORKLOADS["dsa"]
+    rows = [(0, 1.0, None), (1, 1.0, None)]
+    tot = [1000, 100, 50, 100 * w.row_bytes]
+    args = (2, 2, tot, 2.0, (200.0, 200.0), _Res(), rows)
+    ratio = _Env.hbm_peak / bench.HBM_NOMINAL_GBS
+    io = bench.roofline_of(w, {}, _Env(), *args)
+    assert abs(io["hbm_frac_of_nominal"] - io["hbm_frac"] * ratio) <= 1e-12 * io["hbm_frac"]
+    noio = bench.roofline_of(w, {}, _Env(), *args, noio=True)
+    assert abs(noio["frac_of_nominal"] - noio["frac"] * ratio) <= 1e-12 * noio["frac"]
