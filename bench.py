@@ -57,8 +57,22 @@ MLA_SCALE = 1.0 / math.sqrt(192.0)  # softmax scale of the attention consumer: 1
 HEADLINE = ("shared", {"prefetch": True})
 # (workload, mode) of the default run after the headline; modes of one workload are adjacent so its pool is reused
 DEFAULT_SET = [("shared", {"prefetch": True, "prefetch_depth": 2}), ("shared", {"prefetch": True, "prefetch_depth": 4}),
-               ("shared", {"shared_call": True}), ("shared", {"full_offload": True}), ("tiny", {}), ("dsa", {}),
-               ("dsa", {"full_offload": True}), ("multilayer", {}), ("quest", {})]
+               ("shared", {"shared_call": True}), ("shared", {"full_offload": True}),
+               ("shared_own16", {"prefetch": True}), ("tiny", {}), ("dsa", {}), ("dsa", {"full_offload": True}),
+               ("multilayer", {}), ("quest", {})]
+# The headline workload's 78 layers need 429 GB of host pool, so its layers share one pool; a layer reading the pages
+# the previous layer just read (the same tokens, shifted rows) is much faster than one reading a pool of its own. The
+# same pipeline on 16 of its layers, each with a host pool of its own (88 GB), measures the per-layer cost without
+# that reuse.
+OWN_POOL_LAYERS = 16
+
+
+def workload_of(name: str) -> wl.Workload:
+    if name == "shared_own16":
+        import dataclasses
+
+        return dataclasses.replace(wl.WORKLOADS["shared"], layers=OWN_POOL_LAYERS)
+    return wl.WORKLOADS[name]
 HIDING_WORK_MB = 64.0  # per-layer work stand-in of the prefetch-hiding measurement on the headline workload
 # Before a timed pass the stream first runs a spin of this many GPU cycles (about 97 ms at 2.07 GHz), outside the
 # timed intervals: the host then enqueues every step of the pass while the GPU is still busy, so a stall of the host
@@ -101,8 +115,8 @@ def mem_available() -> int:
 
 def choose_host_layers(w: wl.Workload, alias: bool = False) -> int:
     """All layers get their own host pool when it fits in half of the available host memory (and aliasing is not
-    asked for); otherwise every layer reads one shared pool (host_layer_stride 0). Loads use ld.global.cv, so a
-    shared pool still sends every miss over the link."""
+    asked for); otherwise every layer reads one shared pool, shifted per layer (see Resources). Loads use
+    ld.global.cv, so a shared pool still sends every miss over the link."""
     if w.layers == 1:
         return 1
     if alias:
@@ -237,16 +251,21 @@ class Resources:
     whose misses come from an HBM copy of the host pool; the selections of every step in device memory."""
 
     def __init__(self, w: wl.Workload, alias_host: bool = False, noio: bool = True, attention: bool = False,
-                 tiered_frac: float | None = None):
+                 tiered_frac: float | None = None, layer_shift_rows: int | None = None):
         import torch
 
         import hierarchical_sparse_attention_hs_gb300 as hs
 
         self.torch, self.hs, self.w = torch, hs, w
         self.host_layers = choose_host_layers(w, alias_host)
+        # Layers that share one host pool read it shifted by ctx / layers rows per layer, so that layers selecting
+        # the same tokens (a shared selection) read different host rows, as with a pool per layer: re-reading the
+        # rows the previous layer just read is much faster than reading fresh ones.
+        if layer_shift_rows is None:
+            layer_shift_rows = w.ctx // w.layers if self.host_layers == 1 and w.layers > 1 else 0
         self.buf = hs.PoolBuffers(w.layers, w.requests, w.ctx, w.slots, w.topk, w.row_bytes,
-                                  host_layers=self.host_layers, noio=noio)
-        wl.fill_host_pool(w, self.buf.host.ptr, self.host_layers)
+                                  host_layers=self.host_layers, noio=noio, layer_shift_rows=layer_shift_rows)
+        wl.fill_host_pool(w, self.buf.host.ptr, self.host_layers, extra_rows=self.buf.extra_rows)
         self.pool = self.buf.create()
         self.noio_pool = None
         if noio:
@@ -271,7 +290,8 @@ class Resources:
     def host_rows_layer0(self) -> np.ndarray:
         """Layer 0 of the host pool as uint8 [requests][ctx][row_bytes] (a view of the mapped buffer)."""
         w = self.w
-        return self.buf.host.numpy().reshape(self.host_layers, w.requests, w.ctx, w.row_bytes)[0]
+        n = self.host_layers * w.requests * w.ctx * w.row_bytes
+        return self.buf.host.numpy()[:n].reshape(self.host_layers, w.requests, w.ctx, w.row_bytes)[0]
 
     def counters(self) -> np.ndarray:
         return self.buf.view("counters").cpu().numpy().astype(np.int64).sum(axis=0)
@@ -804,7 +824,9 @@ def measure(env: Env, res: Resources, mode: dict, K: int, W: int, legs: set, cpu
         "miss_gbs": int(tot[3]) / (total_ms / 1e3) / 1e9 * env.world,
         "gpu_launches": K * g.launches_per_step(),
         "host_pool": ("one pool per layer" if res.host_layers == w.layers else
-                      "layers share one host pool (host_layer_stride 0); every miss still crosses the link"),
+                      f"layers share one host pool, layer l reading token t from row t + l * "
+                      f"{res.buf.layer_shift_rows} (host_layer_stride = that many rows), so no two layers read the "
+                      f"same row for the same token; every miss crosses the link"),
     }
     out.update(step_stats(rows, w, max(link)))
     out["step_ms"] = [round(r[1], 4) for r in rows]
@@ -1048,7 +1070,7 @@ def gpu_measure(args, env: Env) -> dict:
         head_mode = {k: v for k, v in head_mode.items() if v not in (None, False, 0.0) and
                      not (k == "prefetch_depth" and v == 1)}
         others = []
-    alias = args.workload == "all" or args.alias_host
+    alias = args.alias_host  # otherwise layers share a host pool only where their own pools do not fit
     cache = {}
 
     def resources(name, mode):
@@ -1057,8 +1079,10 @@ def gpu_measure(args, env: Env) -> dict:
             for k in list(cache):
                 cache.pop(k).close()
             torch.cuda.empty_cache()
-            w = wl.WORKLOADS[name]
-            r = Resources(w, alias_host=alias, noio="noio" in legs, attention=bool(mode.get("attention")),
+            w = workload_of(name)
+            # (the own-pool comparison needs no HBM copy of its 88 GB pool: its no-IO mode is the headline's)
+            r = Resources(w, alias_host=alias, noio="noio" in legs and name != "shared_own16",
+                          attention=bool(mode.get("attention")),
                           tiered_frac=mode.get("tiered_frac"))
             # the GPU reads the whole host pool once (as a long-running server has long since done), so that
             # first-touch address translation of host pages is not charged to the timed steps; it also measures

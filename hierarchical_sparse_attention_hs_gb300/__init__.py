@@ -301,12 +301,15 @@ class PoolBuffers:
     """Caller-side memory for one pool, allocated with torch (device) and hs_host_alloc (host), plus the handle.
 
     ``host_layers`` host-pool layers are allocated; with fewer than ``layers`` the pool's layer stride is 0 only
-    when host_layers == 1 (all layers read one pool). ``noio`` keeps a device copy of the host pool and selects
-    the no-IO source. Views of the metadata arrays are exposed as torch tensors for inspection.
+    when host_layers == 1 (all layers read one pool). ``layer_shift_rows`` S > 0 (with host_layers == 1) makes the
+    layer stride S rows instead: the pool grows by (layers - 1) * S rows and layer l reads token t of request b from
+    flat row b * ctx + t + l * S, so layers that select the same tokens read different rows. ``noio`` keeps a
+    device copy of the host pool and selects the no-IO source. Views of the metadata arrays are exposed as torch
+    tensors for inspection.
     """
 
     def __init__(self, layers, max_batch, ctx, slots, topk_max, row_bytes, host_layers=None, noio=False,
-                 host: HostBuffer | None = None, stream=None):
+                 host: HostBuffer | None = None, stream=None, layer_shift_rows: int = 0):
         import torch
 
         self.layers, self.max_batch, self.ctx, self.slots = layers, max_batch, ctx, slots
@@ -314,14 +317,20 @@ class PoolBuffers:
         self.host_layers = layers if host_layers is None else host_layers
         if self.host_layers not in (1, layers):
             raise ValueError("host_layers must be 1 (shared pool) or equal to layers")
+        if layer_shift_rows < 0 or (layer_shift_rows and self.host_layers != 1):
+            raise ValueError("layer_shift_rows applies to a shared host pool only")
+        self.layer_shift_rows = layer_shift_rows if layers > 1 else 0
         per_layer = max_batch * ctx * row_bytes
-        self.host = host if host is not None else HostBuffer(self.host_layers * per_layer)
+        self.extra_rows = (layers - 1) * self.layer_shift_rows
+        host_bytes = self.host_layers * per_layer + self.extra_rows * row_bytes
+        self.host = host if host is not None else HostBuffer(host_bytes)
         self.hot = torch.zeros(layers * max_batch * slots * row_bytes, dtype=torch.uint8, device="cuda")
         self.noio_src = None
         if noio:
-            self.noio_src = torch.empty(self.host_layers * per_layer, dtype=torch.uint8, device="cuda")
-        self.desc = hs_pool_desc(layers, max_batch, ctx, slots, topk_max, row_bytes, self.host.ptr,
-                                 per_layer if self.host_layers == layers else 0, 0, self.hot.data_ptr(), None, None)
+            self.noio_src = torch.empty(host_bytes, dtype=torch.uint8, device="cuda")
+        layer_stride = per_layer if self.host_layers == layers else self.layer_shift_rows * row_bytes
+        self.desc = hs_pool_desc(layers, max_batch, ctx, slots, topk_max, row_bytes, self.host.ptr, layer_stride, 0,
+                                 self.hot.data_ptr(), None, None)
         nbytes = hs_meta_bytes(self.desc)
         if nbytes == 0:
             raise HsError(HS_ERR_INVALID_ARG, "hs_meta_bytes")

@@ -9,10 +9,11 @@ import oracle
 import workload as wl
 
 
-def make_pool(w: wl.Workload, host_layers: int = 1, noio: bool = False, max_batch: int | None = None):
+def make_pool(w: wl.Workload, host_layers: int = 1, noio: bool = False, max_batch: int | None = None,
+              layer_shift_rows: int = 0):
     buf = hs.PoolBuffers(w.layers, max_batch or w.requests, w.ctx, w.slots, w.topk, w.row_bytes,
-                         host_layers=host_layers, noio=noio)
-    wl.fill_host_pool(w, buf.host.ptr, buf.host_layers)
+                         host_layers=host_layers, noio=noio, layer_shift_rows=layer_shift_rows)
+    wl.fill_host_pool(w, buf.host.ptr, buf.host_layers, extra_rows=buf.extra_rows)
     if noio:
         buf.upload_noio()
     buf.create()
@@ -20,7 +21,18 @@ def make_pool(w: wl.Workload, host_layers: int = 1, noio: bool = False, max_batc
 
 
 def host_rows(buf) -> np.ndarray:
-    return buf.host.numpy().reshape(buf.host_layers, buf.max_batch, buf.ctx, buf.row_bytes)
+    n = buf.host_layers * buf.max_batch * buf.ctx * buf.row_bytes
+    return buf.host.numpy()[:n].reshape(buf.host_layers, buf.max_batch, buf.ctx, buf.row_bytes)
+
+
+def layer_rows(buf, l: int, b: int) -> np.ndarray:
+    """The ctx host rows layer l of request b reads: its own pool layer, the shared pool, or the shared pool
+    from row l * layer_shift_rows on."""
+    if buf.host_layers == buf.layers:
+        return host_rows(buf)[l, b]
+    flat = buf.host.numpy().reshape(-1, buf.row_bytes)
+    start = b * buf.ctx + l * buf.layer_shift_rows
+    return flat[start:start + buf.ctx]
 
 
 def check_hot_rows(buf, layers=None) -> None:
@@ -28,15 +40,13 @@ def check_hot_rows(buf, layers=None) -> None:
 
     (The oracle's own hot buffer satisfies exactly this, pinned by invariant I2; slot_tok is compared with the
     oracle separately.)"""
-    host = host_rows(buf)
     st_all = buf.view("slot_tok").cpu().numpy()
     for l in (range(buf.layers) if layers is None else layers):
         hot = buf.hot_view()[l].cpu().numpy()
-        hl = l if buf.host_layers == buf.layers else 0
         for b in range(buf.max_batch):
             st = st_all[l, b]
             occ = st >= 0
-            assert np.array_equal(hot[b][occ], host[hl, b][st[occ]]), (l, b)
+            assert np.array_equal(hot[b][occ], layer_rows(buf, l, b)[st[occ]]), (l, b)
             assert not hot[b][~occ].any(), (l, b)
 
 
@@ -52,12 +62,12 @@ def compare_state(buf, ora: oracle.OraclePool, tag="") -> None:
 
 def replay(w: wl.Workload, steps: int | None = None, host_layers: int = 1, noio: bool = False,
            prefetch: bool = False, graphs: bool = False, mid_check: bool = True, shared_call: bool = False,
-           depth: int = 0, fused: bool = False):
+           depth: int = 0, fused: bool = False, layer_shift_rows: int = 0):
     """Run `steps` decode steps of workload w on the GPU and in the oracle; compare out_slots after every step
     and the whole state at the midpoint and at the end. Returns (buf, oracle pool)."""
     ns = w.steps if steps is None else steps
     sel = wl.gen_selections(w, steps=ns)  # [ns][selection layers][B][k]
-    buf = make_pool(w, host_layers=host_layers, noio=noio)
+    buf = make_pool(w, host_layers=host_layers, noio=noio, layer_shift_rows=layer_shift_rows)
     pool = buf.handle
     L, B, k = w.layers, w.requests, w.topk
     ora = oracle.OraclePool(w.ctx, w.slots, w.row_bytes, L, B, track_rows=False)

@@ -81,6 +81,21 @@ def test_shared_prefetch_in_graph():
     buf.close()
 
 
+@pytest.mark.parametrize("shared_call", [False, True])
+def test_shared_pool_read_with_a_layer_shift_is_exact(shared_call):
+    # one host pool for all layers, layer l reading token t from row t + l * S (the benchmark's stand-in for a pool
+    # per layer): the state equals the oracle's, and every layer's hot rows are its own shifted host rows
+    w = wl.WORKLOADS["shared"]
+    shift = w.ctx // w.layers
+    if shared_call:
+        buf, _ = gh.replay(w, steps=4, shared_call=True, layer_shift_rows=shift)
+    else:
+        buf, _ = gh.replay(w, steps=4, prefetch=True, graphs=True, depth=1, layer_shift_rows=shift)
+    assert buf.layer_shift_rows == shift and buf.desc.host_layer_stride == shift * w.row_bytes
+    gh.check_hot_rows(buf, layers=[0, 1, 40, 77])
+    buf.close()
+
+
 def test_shared_selection_one_call_for_all_layers():
     # hs_resolve_shared: one resolve per step drives all 78 layers; state, counters and rows equal the oracle's
     # per-layer resolves

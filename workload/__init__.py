@@ -154,11 +154,14 @@ def rows(w: Workload, layer: int, request: int, tok0: int = 0, ntok: int | None 
     return out
 
 
-def fill_host_pool(w: Workload, address: int, host_layers: int, threads: int | None = None) -> None:
-    """Fill a host pool laid out [host_layers][requests][ctx][row_bytes] at raw address `address`.
+def fill_host_pool(w: Workload, address: int, host_layers: int, threads: int | None = None,
+                   extra_rows: int = 0) -> None:
+    """Fill a host pool laid out [host_layers][requests][ctx][row_bytes] at raw address `address`, followed by
+    `extra_rows` more rows (a shared pool read with a per-layer shift reaches past its last request's rows).
 
     Layer l of the pool holds the rows of layer l (host_layers == layers) or, when layers alias a smaller pool,
-    of pool layer l. Filled in parallel chunks (the C routine releases the GIL through ctypes).
+    of pool layer l; the extra rows hold rows ctx, ctx + 1, ... of the last request of the last pool layer.
+    Filled in parallel chunks (the C routine releases the GIL through ctypes).
     """
     per_rl = w.ctx * w.row_bytes
     jobs = [(l, b) for l in range(host_layers) for b in range(w.requests)]
@@ -170,6 +173,9 @@ def fill_host_pool(w: Workload, address: int, host_layers: int, threads: int | N
         for t0 in range(0, w.ctx, chunk):
             n = min(chunk, w.ctx - t0)
             tasks.append((l, b, t0, n))
+    # rows ctx .. of (last layer, last request) continue the pool contiguously
+    for t0 in range(w.ctx, w.ctx + extra_rows, chunk):
+        tasks.append((host_layers - 1, w.requests - 1, t0, min(chunk, w.ctx + extra_rows - t0)))
 
     def worker(idx):
         for i in range(idx, len(tasks), nthreads):
