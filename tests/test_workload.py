@@ -77,3 +77,22 @@ def test_tiny_rows_are_bf16_standard_normal():
     vals = (r.view(np.uint16).astype(np.uint32) << 16).view(np.float32)
     assert vals.shape == (w.ctx, w.row_bytes // 2)
     assert abs(vals.mean()) < 0.01 and abs(vals.std() - 1.0) < 0.01
+
+
+def test_host_pool_extra_rows_continue_the_last_request():
+    """A shared pool read with a per-layer shift reaches past its last request's rows: the extra rows are rows ctx,
+    ctx + 1, ... of that request, written right after its row ctx - 1."""
+    import dataclasses
+
+    w = dataclasses.replace(wl.WORKLOADS["dsa"], requests=2, ctx=1024)
+    extra = 37
+    pool = np.zeros((w.requests * w.ctx + extra, w.row_bytes), dtype=np.uint8)
+    wl.fill_host_pool(w, pool.ctypes.data, 1, threads=3, extra_rows=extra)
+    for b in range(w.requests):
+        assert np.array_equal(pool[b * w.ctx:(b + 1) * w.ctx], wl.rows(w, 0, b))
+    assert np.array_equal(pool[w.requests * w.ctx:], wl.rows(w, 0, w.requests - 1, w.ctx, extra))
+    # a layer shifted by s rows reads, for token t of request b, the row of token t + s (past the end: the extra rows)
+    s = 29
+    flat = pool.reshape(-1, w.row_bytes)
+    t = w.ctx - 5
+    assert np.array_equal(flat[(w.requests - 1) * w.ctx + t + s], wl.rows(w, 0, w.requests - 1, t + s, 1)[0])
