@@ -645,9 +645,9 @@ def e2e_passes(res: Resources, mode: dict, k_steps: int, ref_graphs: StepGraphs)
 
 
 def _oracle_requests(w: wl.Workload, lo: int, hi: int, sel: np.ndarray, host: np.ndarray, res, budget_s: float,
-                     t0: float) -> tuple:
-    """Steps of layer 0 for requests lo..hi-1 from the cold start, the sequence replayed from a fresh cache each
-    time it ends (as the GPU passes do), until the budget; (selections, steps)."""
+                     t0: float, ls: int = 0) -> tuple:
+    """Steps of one layer (selection layer ls) for requests lo..hi-1 from the cold start, the sequence replayed from a
+    fresh cache each time it ends (as the GPU passes do), until the budget; (selections, steps)."""
     import oracle
 
     n = steps = 0
@@ -657,7 +657,7 @@ def _oracle_requests(w: wl.Workload, lo: int, hi: int, sel: np.ndarray, host: np
             if time.perf_counter() - t0 >= budget_s:
                 break
             pool.step_begin()
-            pool.resolve(0, sel[s, 0, lo:hi], host[lo:hi], resident=None if res is None else res[s, lo:hi])
+            pool.resolve(0, sel[s, ls, lo:hi], host[lo:hi], resident=None if res is None else res[s, lo:hi])
             n += hi - lo
             steps += 1
     return n, steps
@@ -666,22 +666,29 @@ def _oracle_requests(w: wl.Workload, lo: int, hi: int, sel: np.ndarray, host: np
 def cpu_baseline(w: wl.Workload, budget_s: float = 12.0, tiered_frac: float | None = None, threads: int = 1,
                  host: np.ndarray | None = None) -> dict:
     """The CPU oracle on a bounded sample of the same workload: request-layers of layer 0, hot rows tracked in
-    host memory, steps in order from the cold start until the time budget. With threads > 1 the requests are
+    host memory, steps in order from the cold start until the time budget. With threads > 1 the request-layers are
     split over that many threads (the oracle's C routine runs without the interpreter lock), each resolving its
-    own requests, which are independent. `host` is layer 0's host rows [requests][ctx][row_bytes] (generated when
-    not given)."""
+    own, which are independent: the requests of layer 0, and with more threads than requests whole layers of
+    requests (threads // requests layers, one request-layer per thread; their rows are layer 0's, which costs the
+    same). `host` is layer 0's host rows [requests][ctx][row_bytes] (generated when not given)."""
     reqs = w.requests
-    sel = wl.gen_selections(w, layers=(0, 1), requests=(0, reqs))
+    nl = max(1, min(w.layers, threads // reqs)) if threads > reqs else 1
+    sel = wl.gen_selections(w, layers=(0, 1 if w.shared_across_layers else nl), requests=(0, reqs))
     if host is None:
         host = np.stack([wl.rows(w, 0, b) for b in range(reqs)])
     res = None if tiered_frac is None else wl.gen_resident(w.ctx, reqs, w.steps, w.seed, frac=tiered_frac)
-    threads = max(1, min(threads, reqs))
-    bounds = [reqs * i // threads for i in range(threads + 1)]
+    if nl > 1:  # one request-layer per thread
+        units = [(0 if w.shared_across_layers else l, b, b + 1) for l in range(nl) for b in range(reqs)]
+    else:
+        th = max(1, min(threads, reqs))
+        units = [(0, reqs * i // th, reqs * (i + 1) // th) for i in range(th)]
+    threads = len(units)
     results = [None] * threads
     t0 = time.perf_counter()
 
     def work(i):
-        results[i] = _oracle_requests(w, bounds[i], bounds[i + 1], sel, host, res, budget_s, t0)
+        ls, lo, hi = units[i]
+        results[i] = _oracle_requests(w, lo, hi, sel, host, res, budget_s, t0, ls)
 
     ths = [threading.Thread(target=work, args=(i,)) for i in range(threads)]
     for t in ths:
@@ -691,9 +698,11 @@ def cpu_baseline(w: wl.Workload, budget_s: float = 12.0, tiered_frac: float | No
     dt = time.perf_counter() - t0
     n = sum(r[0] for r in results)
     steps = min(r[1] for r in results)
-    how = "single-threaded" if threads == 1 else f"{threads} threads over the requests"
+    how = ("single-threaded" if threads == 1 else
+           f"{threads} threads, one request-layer each" if nl > 1 else f"{threads} threads over the requests")
+    which = f"layers 0..{nl - 1}" if nl > 1 else "layer 0"
     return {"value": n / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"layer 0 of {w.name}, {reqs} requests, at least {steps} decode steps (the {w.steps}-step "
+            "sample": f"{which} of {w.name}, {reqs} requests, at least {steps} decode steps (the {w.steps}-step "
                       f"sequence replayed from the cold start; {n} selections, hot rows tracked" +
                       (", resident maps" if res is not None else "") + f", {dt:.1f} s {how})"}
 
@@ -884,7 +893,7 @@ def measure(env: Env, res: Resources, mode: dict, K: int, W: int, legs: set, cpu
         host = res.host_rows_layer0()
         tiered = mode.get("tiered_frac")
         out["cpu_baseline"] = cpu_baseline(w, budget_s=cpu_budget, tiered_frac=tiered, host=host)
-        if headline and min(cpu_threads, w.requests) > 1:
+        if headline and cpu_threads > 1:
             out["cpu_baseline_threads"] = cpu_baseline(w, budget_s=cpu_budget, tiered_frac=tiered,
                                                        threads=cpu_threads, host=host)
     return out
