@@ -1,5 +1,6 @@
-"""bench.py's traffic bookkeeping on CPU: a committed ncu capture counts only while the kernel sources it was taken
-on are unchanged (the hash it records matches), otherwise the bench line reports null."""
+"""bench.py's host-side bookkeeping on CPU: a committed ncu capture counts only while the kernel sources it was
+taken on are unchanged (the hash it records matches), otherwise the bench line reports null; the roofline fractions
+against the measured and nominal peaks; the CPU oracle's thread split; the own-pool entry's workload."""
 import json
 
 import bench
@@ -98,3 +99,26 @@ def test_hbm_fractions_against_measured_and_nominal_peaks():
     assert abs(io["hbm_frac_of_nominal"] - io["hbm_frac"] * ratio) <= 1e-12 * io["hbm_frac"]
     noio = bench.roofline_of(w, {}, _Env(), *args, noio=True)
     assert abs(noio["frac_of_nominal"] - noio["frac"] * ratio) <= 1e-12 * noio["frac"]
+
+
+def test_threaded_cpu_baseline_spreads_over_request_layers():
+    """With more threads than requests the CPU oracle runs one request-layer per thread, several layers of requests
+    (a workload with its own selection per layer reads each layer's)."""
+    import dataclasses
+
+    w = dataclasses.replace(wl.WORKLOADS["tiny"], requests=2, layers=4, ctx=512, slots=128, topk=16, steps=4)
+    many = bench.cpu_baseline(w, budget_s=0.3, threads=8)
+    assert many["cores"] == 8 and "layers 0..3" in many["sample"] and many["value"] > 0
+    few = bench.cpu_baseline(w, budget_s=0.3, threads=2)
+    assert few["cores"] == 2 and "layer 0 " in few["sample"]
+    one = bench.cpu_baseline(w, budget_s=0.3, threads=1)
+    assert one["cores"] == 1 and "single-threaded" in one["sample"]
+
+
+def test_own_pool_entry_is_the_headline_workload_on_fewer_layers():
+    w = bench.workload_of("shared_own16")
+    head = wl.WORKLOADS[bench.HEADLINE[0]]
+    assert w.layers == bench.OWN_POOL_LAYERS < head.layers
+    assert (w.requests, w.ctx, w.topk, w.slots, w.row_bytes, w.shared_across_layers) == (
+        head.requests, head.ctx, head.topk, head.slots, head.row_bytes, head.shared_across_layers)
+    assert ("shared_own16", {"prefetch": True}) in bench.DEFAULT_SET
