@@ -32,6 +32,7 @@ the barrier and the max-over-ranks time). ``--impl reference`` times the CPU ora
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -65,14 +66,6 @@ DEFAULT_SET = [("shared", {"prefetch": True, "prefetch_depth": 2}), ("shared", {
 # same pipeline on 16 of its layers, each with a host pool of its own (88 GB), measures the per-layer cost without
 # that reuse.
 OWN_POOL_LAYERS = 16
-
-
-def workload_of(name: str) -> wl.Workload:
-    if name == "shared_own16":
-        import dataclasses
-
-        return dataclasses.replace(wl.WORKLOADS["shared"], layers=OWN_POOL_LAYERS)
-    return wl.WORKLOADS[name]
 HIDING_WORK_MB = 64.0  # per-layer work stand-in of the prefetch-hiding measurement on the headline workload
 # Before a timed pass the stream first runs a spin of this many GPU cycles (about 97 ms at 2.07 GHz), outside the
 # timed intervals: the host then enqueues every step of the pass while the GPU is still busy, so a stall of the host
@@ -83,6 +76,13 @@ HIDING_WORK_MB = 64.0  # per-layer work stand-in of the prefetch-hiding measurem
 # and the host blocks before it can release, and first launches wait for the device to go idle.)
 LEAD_CYCLES = 200_000_000
 HBM_NOMINAL_GBS = 8000.0  # the nominal HBM3e rate ("about 8 TB/s"), reported beside the measured copy peak
+
+
+def workload_of(name: str) -> wl.Workload:
+    """A workload by name; `shared_own16` is the headline workload on OWN_POOL_LAYERS layers."""
+    if name == "shared_own16":
+        return dataclasses.replace(wl.WORKLOADS["shared"], layers=OWN_POOL_LAYERS)
+    return wl.WORKLOADS[name]
 
 
 def describe(w: wl.Workload) -> str:
@@ -259,8 +259,9 @@ class Resources:
         self.torch, self.hs, self.w = torch, hs, w
         self.host_layers = choose_host_layers(w, alias_host)
         # Layers that share one host pool read it shifted by ctx / layers rows per layer, so that layers selecting
-        # the same tokens (a shared selection) read different host rows, as with a pool per layer: re-reading the
-        # rows the previous layer just read is much faster than reading fresh ones.
+        # the same tokens (a shared selection) read different host rows, as with a pool per layer. They still read
+        # largely the same host pages, which keeps their fetches faster than a pool per layer's (the translation of
+        # host addresses bounds scattered rows); the own-pool entry of the default run measures the difference.
         if layer_shift_rows is None:
             layer_shift_rows = w.ctx // w.layers if self.host_layers == 1 and w.layers > 1 else 0
         self.buf = hs.PoolBuffers(w.layers, w.requests, w.ctx, w.slots, w.topk, w.row_bytes,
