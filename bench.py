@@ -56,16 +56,16 @@ UNIT = "selections/s"
 FLUSH_BYTES = 256 << 20
 MLA_SCALE = 1.0 / math.sqrt(192.0)  # softmax scale of the attention consumer: 1/sqrt(128 + 64)
 HEADLINE = ("shared", {"prefetch": True})
-# (workload, mode) of the default run after the headline; modes of one workload are adjacent so its pool is reused
-DEFAULT_SET = [("shared", {"prefetch": True, "prefetch_depth": 2}), ("shared", {"prefetch": True, "prefetch_depth": 4}),
-               ("shared", {"shared_call": True}), ("shared", {"full_offload": True}),
-               ("shared_own16", {"prefetch": True}), ("tiny", {}), ("dsa", {}), ("dsa", {"full_offload": True}),
-               ("multilayer", {}), ("quest", {})]
 # The headline workload's 78 layers need 429 GB of host pool, so its layers share one pool; a layer reading the pages
 # the previous layer just read (the same tokens, shifted rows) is much faster than one reading a pool of its own. The
 # same pipeline on 16 of its layers, each with a host pool of its own (88 GB), measures the per-layer cost without
 # that reuse.
 OWN_POOL_LAYERS = 16
+# (workload, mode) of the default run after the headline; modes of one workload are adjacent so its pool is reused
+DEFAULT_SET = [("shared", {"prefetch": True, "prefetch_depth": 2}), ("shared", {"prefetch": True, "prefetch_depth": 4}),
+               ("shared", {"shared_call": True}), ("shared", {"full_offload": True}),
+               (f"shared_own{OWN_POOL_LAYERS}", {"prefetch": True}), ("tiny", {}), ("dsa", {}), ("dsa", {"full_offload": True}),
+               ("multilayer", {}), ("quest", {})]
 HIDING_WORK_MB = 64.0  # per-layer work stand-in of the prefetch-hiding measurement on the headline workload
 # Before a timed pass the stream first runs a spin of this many GPU cycles (about 97 ms at 2.07 GHz), outside the
 # timed intervals: the host then enqueues every step of the pass while the GPU is still busy, so a stall of the host
@@ -79,9 +79,10 @@ HBM_NOMINAL_GBS = 8000.0  # the nominal HBM3e rate ("about 8 TB/s"), reported be
 
 
 def workload_of(name: str) -> wl.Workload:
-    """A workload by name; `shared_own16` is the headline workload on OWN_POOL_LAYERS layers."""
-    if name == "shared_own16":
-        return dataclasses.replace(wl.WORKLOADS["shared"], layers=OWN_POOL_LAYERS)
+    """A workload by name; `shared_own<N>` is the headline workload on N layers (each with a host pool of its own
+    wherever they fit)."""
+    if name.startswith("shared_own") and name[len("shared_own"):].isdigit():
+        return dataclasses.replace(wl.WORKLOADS["shared"], layers=int(name[len("shared_own"):]))
     return wl.WORKLOADS[name]
 
 
@@ -1072,7 +1073,7 @@ def gpu_measure(args, env: Env) -> dict:
         head_name, head_mode = HEADLINE
         others = [] if args.headline_only else DEFAULT_SET
     else:
-        head_name = args.workload
+        head_name = args.workload if not args.own_pool_layers else f"shared_own{args.own_pool_layers}"
         head_mode = {"prefetch": args.prefetch, "prefetch_depth": args.prefetch_depth if args.prefetch else 1,
                      "shared_call": args.shared_call,
                      "layer_work_mb": args.layer_work_mb, "work_only": args.work_only,
@@ -1091,7 +1092,7 @@ def gpu_measure(args, env: Env) -> dict:
             torch.cuda.empty_cache()
             w = workload_of(name)
             # (the own-pool comparison needs no HBM copy of its 88 GB pool: its no-IO mode is the headline's)
-            r = Resources(w, alias_host=alias, noio="noio" in legs and name != "shared_own16",
+            r = Resources(w, alias_host=alias, noio="noio" in legs and not name.startswith("shared_own"),
                           attention=bool(mode.get("attention")),
                           tiered_frac=mode.get("tiered_frac"))
             # the GPU reads the whole host pool once (as a long-running server has long since done), so that
@@ -1128,7 +1129,7 @@ def gpu_measure(args, env: Env) -> dict:
             attention = {"error": f"{type(e).__name__}: {e}"}
     for k in list(cache):
         cache.pop(k).close()
-    w = wl.WORKLOADS[head_name]
+    w = workload_of(head_name)
     line = {
         "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": env.world, "steps": K, "warmup": W,
         "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -1209,6 +1210,8 @@ def parse_args(argv=None):
     ap.add_argument("--legs", default="io,floor,e2e,noio,cpu,spread,hiding,attention",
                     help="comma-separated legs: floor, e2e, noio, cpu, spread, hiding, attention")
     ap.add_argument("--alias-host", action="store_true", help="all layers read one host pool")
+    ap.add_argument("--own-pool-layers", type=int, default=0,
+                    help="with --workload shared: that many of its layers, each with a host pool of its own")
     ap.add_argument("--prefetch", action="store_true", help="layer-wise prefetch on a second stream")
     ap.add_argument("--prefetch-depth", type=int, default=1,
                     help="with --prefetch: prefetch this many layers ahead, on as many side streams")
@@ -1240,6 +1243,8 @@ def parse_args(argv=None):
     if args.attention and (args.tiered_frac is not None or args.full_offload or args.work_only):
         ap.error("--attention reads the slot lists of plain resolves; it combines with none of --tiered-frac, "
                  "--full-offload, --work-only")
+    if args.own_pool_layers and (args.workload != "shared" or args.own_pool_layers < 2):
+        ap.error("--own-pool-layers takes --workload shared and at least 2 layers")
     if args.tiered_frac is not None and (args.prefetch or args.shared_call or args.full_offload):
         ap.error("--tiered-frac resolves each layer with its own call; it combines with none of --prefetch, "
                  "--shared-call, --full-offload")
