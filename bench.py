@@ -64,8 +64,8 @@ OWN_POOL_LAYERS = 16
 # (workload, mode) of the default run after the headline; modes of one workload are adjacent so its pool is reused
 DEFAULT_SET = [("shared", {"prefetch": True, "prefetch_depth": 2}), ("shared", {"prefetch": True, "prefetch_depth": 4}),
                ("shared", {"shared_call": True}), ("shared", {"full_offload": True}),
-               (f"shared_own{OWN_POOL_LAYERS}", {"prefetch": True}), ("tiny", {}), ("dsa", {}), ("dsa", {"full_offload": True}),
-               ("multilayer", {}), ("quest", {})]
+               (f"shared_own{OWN_POOL_LAYERS}", {"prefetch": True}), ("tiny", {}), ("dsa", {}),
+               ("dsa", {"full_offload": True}), ("multilayer", {}), ("quest", {})]
 HIDING_WORK_MB = 64.0  # per-layer work stand-in of the prefetch-hiding measurement on the headline workload
 # Before a timed pass the stream first runs a spin of this many GPU cycles (about 97 ms at 2.07 GHz), outside the
 # timed intervals: the host then enqueues every step of the pass while the GPU is still busy, so a stall of the host
@@ -261,8 +261,8 @@ class Resources:
         self.host_layers = choose_host_layers(w, alias_host)
         # Layers that share one host pool read it shifted by ctx / layers rows per layer, so that layers selecting
         # the same tokens (a shared selection) read different host rows, as with a pool per layer. They still read
-        # largely the same host pages, which keeps their fetches faster than a pool per layer's (the translation of
-        # host addresses bounds scattered rows); the own-pool entry of the default run measures the difference.
+        # largely the same host pages, which keeps their fetches faster than a pool per layer's (scattered rows are
+        # bound on the host's side, most likely by address translation); the own-pool entry measures the difference.
         if layer_shift_rows is None:
             layer_shift_rows = w.ctx // w.layers if self.host_layers == 1 and w.layers > 1 else 0
         self.buf = hs.PoolBuffers(w.layers, w.requests, w.ctx, w.slots, w.topk, w.row_bytes,

@@ -88,8 +88,9 @@ typedef struct hs_pool hs_pool;
  *   host_layer_stride: bytes between layers; 0 lets every layer read one shared pool, and a stride smaller than
  *     a layer makes the layers' rows overlap (for benchmarks whose full history does not fit in host memory: a
  *     stride of a few rows gives layers with the same selection different rows to fetch). Multiple of 16, >= 0.
- *     Scattered rows arrive more slowly the more host memory a step's layers spread them over (the translation
- *     of host addresses, not the link, bounds them), so shared or overlapping pools measure an optimistic step.
+ *     Scattered rows arrive more slowly the more host memory a step's layers spread them over (the host's side
+ *     of the fetch, most likely address translation, bounds them, not the link), so shared or overlapping pools
+ *     measure an optimistic step.
  *   host_req_stride: bytes between requests; 0 means ctx*row_bytes. Multiple of 16.
  *   hot_buf: device memory [layers][max_batch][slots][row_bytes], 16-byte aligned. Not initialised here.
  *   meta: device memory of hs_meta_bytes(desc) bytes, 256-byte aligned, holding the metadata arrays, the step
